@@ -1,0 +1,169 @@
+/*
+ * CPU oracle for the batched Walsh-Hadamard transform.  TEST INFRASTRUCTURE ONLY:
+ * nothing in the product library links, loads or calls this file.  Only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg use it.
+ *
+ * What it computes (per real vector x of length N = 2^n):
+ *
+ *     y[k] = s * sum_{i=0}^{N-1} (-1)^{popc(k & i)} x[i]
+ *
+ * with s = 2^{-n/2} for the normalised transform and s = 1 otherwise.  The sign
+ * rule (-1)^{popc(k & i)} is the one stated in "[QDP] [feature] Pr4 kronecker
+ * fwt", section "How" (naive GEMM placeholder); the scale 2^{-n/2} is the usual
+ * orthonormal scaling of H_n.
+ *
+ * Two routines:
+ *   - oracle_fwt_f64 / oracle_fwt_u32: the textbook in-place butterfly network,
+ *     stage h pairing entries at distance 1, 2, 4, ... with (a+b, a-b), as in the
+ *     iThome "Day 18" FWT post, section "Tensor Core wants matrix
+ *     multiplication" (stage 0 local pairs, stage 1 stride 2, stage 2 stride 4).
+ *     Floating point runs in double; int32 runs in uint32_t so that overflow
+ *     wraps modulo 2^32 (signed overflow is undefined in C).
+ *   - oracle_fwt_entry_f64 / oracle_fwt_entry_u32: one output entry straight from
+ *     the definition above, O(N) per entry, for spot checks at sizes where the
+ *     whole reference transform is too slow to repeat.
+ *
+ * No blocking, no fusion, no reordering: one stage after another over the whole
+ * vector.  Threads (plain pthreads) only split the batch into whole vectors.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* s = 2^{-n/2} in double; 1 when not normalising. */
+double oracle_scale(int n, int normalize) {
+  if (!normalize) return 1.0;
+  if (n % 2 == 0) return ldexp(1.0, -n / 2);
+  return ldexp(1.0, -(n - 1) / 2) / sqrt(2.0);
+}
+
+static void butterfly_f64(double* x, int64_t N) {
+  for (int64_t h = 1; h < N; h *= 2) {
+    for (int64_t i = 0; i < N; i += 2 * h) {
+      for (int64_t j = i; j < i + h; ++j) {
+        double u = x[j];
+        double v = x[j + h];
+        x[j] = u + v;
+        x[j + h] = u - v;
+      }
+    }
+  }
+}
+
+static void butterfly_u32(uint32_t* x, int64_t N) {
+  for (int64_t h = 1; h < N; h *= 2) {
+    for (int64_t i = 0; i < N; i += 2 * h) {
+      for (int64_t j = i; j < i + h; ++j) {
+        uint32_t u = x[j];
+        uint32_t v = x[j + h];
+        x[j] = u + v;
+        x[j + h] = u - v;
+      }
+    }
+  }
+}
+
+typedef struct {
+  const void* x;
+  void* y;
+  int n;
+  int64_t first, last; /* vectors [first, last) */
+  double scale;
+  int is_int;
+} job_t;
+
+static void* run_job(void* arg) {
+  job_t* jb = (job_t*)arg;
+  int64_t N = (int64_t)1 << jb->n;
+  for (int64_t b = jb->first; b < jb->last; ++b) {
+    if (jb->is_int) {
+      const uint32_t* src = (const uint32_t*)jb->x + b * N;
+      uint32_t* dst = (uint32_t*)jb->y + b * N;
+      if (dst != src) memcpy(dst, src, (size_t)N * sizeof(uint32_t));
+      butterfly_u32(dst, N);
+    } else {
+      const double* src = (const double*)jb->x + b * N;
+      double* dst = (double*)jb->y + b * N;
+      if (dst != src) memcpy(dst, src, (size_t)N * sizeof(double));
+      butterfly_f64(dst, N);
+      if (jb->scale != 1.0)
+        for (int64_t k = 0; k < N; ++k) dst[k] *= jb->scale;
+    }
+  }
+  return NULL;
+}
+
+static int run_batch(const void* x, void* y, int n, int64_t count, double scale,
+                     int is_int, int nthreads) {
+  if (n < 0 || n > 40 || count < 0 || (count > 0 && (!x || !y))) return 1;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > count) nthreads = count > 0 ? (int)count : 1;
+  job_t* jobs = (job_t*)calloc((size_t)nthreads, sizeof(job_t));
+  pthread_t* tids = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  if (!jobs || !tids) { free(jobs); free(tids); return 2; }
+  for (int t = 0; t < nthreads; ++t) {
+    jobs[t].x = x; jobs[t].y = y; jobs[t].n = n; jobs[t].scale = scale;
+    jobs[t].is_int = is_int;
+    jobs[t].first = count * t / nthreads;
+    jobs[t].last = count * (t + 1) / nthreads;
+  }
+  /* A thread that could not be started has its share run on the calling thread. */
+  char* started = (char*)calloc((size_t)nthreads, 1);
+  if (!started) { free(jobs); free(tids); return 2; }
+  for (int t = 1; t < nthreads; ++t)
+    started[t] = pthread_create(&tids[t], NULL, run_job, &jobs[t]) == 0;
+  run_job(&jobs[0]);
+  for (int t = 1; t < nthreads; ++t) {
+    if (started[t]) pthread_join(tids[t], NULL);
+    else run_job(&jobs[t]);
+  }
+  free(started); free(jobs); free(tids);
+  return 0;
+}
+
+/* count vectors of 2^n doubles, x -> y (y may equal x).  Returns 0 on success. */
+int oracle_fwt_f64(const double* x, double* y, int n, int64_t count, int normalize,
+                   int nthreads) {
+  return run_batch(x, y, n, count, oracle_scale(n, normalize), 0, nthreads);
+}
+
+/* count vectors of 2^n uint32 (int32 bit patterns), wrap-around arithmetic. */
+int oracle_fwt_u32(const uint32_t* x, uint32_t* y, int n, int64_t count, int nthreads) {
+  return run_batch(x, y, n, count, 1.0, 1, nthreads);
+}
+
+/* Parity of popc(v): XOR-fold the 64 bits down to one. */
+static int popc_parity(uint64_t v) {
+  v ^= v >> 32; v ^= v >> 16; v ^= v >> 8; v ^= v >> 4; v ^= v >> 2; v ^= v >> 1;
+  return (int)(v & 1u);
+}
+
+/* y[k] of one vector, straight from the definition, then scaled.  The 2^n signed
+ * terms are added with Neumaier's compensated summation (Neumaier 1974), so the
+ * sum is good to a few ulps even at n = 24, where a plain running sum of 2^24
+ * terms could drift far beyond a 1e-12 relative error. */
+double oracle_fwt_entry_f64(const double* x, int n, int64_t k, int normalize) {
+  int64_t N = (int64_t)1 << n;
+  double sum = 0.0, comp = 0.0;
+  for (int64_t i = 0; i < N; ++i) {
+    double t = popc_parity((uint64_t)(k & i)) ? -x[i] : x[i];
+    double s2 = sum + t;
+    if (fabs(sum) >= fabs(t)) comp += (sum - s2) + t;
+    else comp += (t - s2) + sum;
+    sum = s2;
+  }
+  return (sum + comp) * oracle_scale(n, normalize);
+}
+
+/* y[k] of one int32 vector from the definition, modulo 2^32. */
+uint32_t oracle_fwt_entry_u32(const uint32_t* x, int n, int64_t k) {
+  int64_t N = (int64_t)1 << n;
+  uint32_t acc = 0;
+  for (int64_t i = 0; i < N; ++i) {
+    if (popc_parity((uint64_t)(k & i))) acc -= x[i];
+    else acc += x[i];
+  }
+  return acc;
+}

@@ -1,0 +1,64 @@
+"""Plant plausible mistakes in a copy of the oracle and check that a pin catches each.
+
+The mistakes are planted in the oracle's C source on the CPU (a temporary copy,
+compiled with gcc); the real oracle is never touched.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+# (name, original text, replacement, which occurrence (0-based)) -- occurrence 0 of the
+# butterfly lines is the double routine, occurrence 1 the uint32 routine.
+MUTANTS = [
+    ("f64 swapped outputs", "x[j] = u + v;\n        x[j + h] = u - v;",
+     "x[j] = u - v;\n        x[j + h] = u + v;", 0),
+    ("f64 wrong sign", "x[j + h] = u - v;", "x[j + h] = v - u;", 0),
+    ("f64 dropped stage 0", "for (int64_t h = 1; h < N; h *= 2)", "for (int64_t h = 2; h < N; h *= 2)", 0),
+    ("f64 last stage missing", "for (int64_t h = 1; h < N; h *= 2)", "for (int64_t h = 1; 2 * h < N; h *= 2)", 0),
+    ("f64 wrong partner", "double v = x[j + h];", "double v = x[i + h + (j - i + 1) % h];", 0),
+    ("u32 wrong sign", "x[j + h] = u - v;", "x[j + h] = v - u;", 1),
+    ("u32 dropped stage", "for (int64_t h = 1; h < N; h *= 2)", "for (int64_t h = 2; h < N; h *= 2)", 1),
+    ("even scale wrong", "return ldexp(1.0, -n / 2);", "return ldexp(1.0, -n);", 0),
+    ("odd scale inverted", "/ sqrt(2.0);", "* sqrt(2.0);", 0),
+    ("entry uses OR", "double t = popc_parity((uint64_t)(k & i))", "double t = popc_parity((uint64_t)(k | i))", 0),
+    ("int entry transposed sign", "if (popc_parity((uint64_t)(k & i))) acc -= x[i];",
+     "if (!popc_parity((uint64_t)(k & i))) acc -= x[i];", 0),
+    ("scale skipped", "if (jb->scale != 1.0)", "if (jb->scale == 12345.0)", 0),
+]
+
+
+def _replace_nth(text, old, new, nth):
+    start = -1
+    for _ in range(nth + 1):
+        start = text.find(old, start + 1)
+        assert start >= 0, f"mutation anchor not found: {old!r}"
+    return text[:start] + new + text[start + len(old):]
+
+
+@pytest.mark.parametrize("name,old,new,nth", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new, nth):
+    src = open(oracle.SOURCE).read()
+    mutated = _replace_nth(src, old, new, nth)
+    assert mutated != src
+    path = tmp_path / "mutant.c"
+    path.write_text(mutated)
+    so = oracle.compile_library(str(path), str(tmp_path / "libmutant.so"))
+    orc = oracle.Oracle(so)
+    caught = []
+    for pin in oracle_pins.ORACLE_PINS:
+        try:
+            pin(orc)
+        except AssertionError as e:  # the planted mistake was seen
+            caught.append((pin.__name__, str(e)))
+    assert caught, f"no pin caught the planted mistake {name!r}"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    so = oracle.compile_library(oracle.SOURCE, str(tmp_path / "libcopy.so"))
+    orc = oracle.Oracle(so)
+    for pin in oracle_pins.ORACLE_PINS:
+        pin(orc)
+    assert os.path.exists(so)
