@@ -1,0 +1,459 @@
+#!/usr/bin/env python3
+"""Throughput of the batched Walsh-Hadamard transform on GB300.
+
+Metric: FWT vectors/s (plus effective and per-kernel HBM GB/s against the
+measured copy bandwidth).  One step = one full transform of every vector of the
+workload's batch, with inputs resident in HBM.  The default workload is the
+largest specified one, n = 24 (2^24 amplitudes), batch 16, split complex fp64
+*and* the same states in split complex fp32 (6 GiB of input, out of place), the
+multi-pass Kronecker path.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, timed the same way
+
+Multi-GPU runs (torchrun, one rank per GPU) replicate the per-rank workload
+with no collective on the data path (weak scaling); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FWT vectors/sec and achieved HBM GB/s vs n (fraction of GB300 ~8 TB/s peak)"
+UNIT = "vectors/s"
+FALLBACK_HBM_GBS = 6800.0
+# named step workloads: each is a list of input shapes transformed once per step
+STEP_WORKLOADS = {
+    "n24_b16": ["n24_b16_c64", "n24_b16_c32"],
+    "n18_b256_i32": ["n18_b256_i32"],
+    "n14_b64_c32": ["n14_b64_c32"],
+    "n12_b64_c32": ["n12_b64_c32"],
+    "n10_b64_c32": ["n10_b64_c32"],
+    "n24_b16_c64": ["n24_b16_c64"],
+    "n24_b16_c32": ["n24_b16_c32"],
+}
+DEFAULT_WORKLOAD = "n24_b16"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(STEP_WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=8,
+                    help="vectors per part in the cpu_baseline sample of our arm")
+    ap.add_argument("--ref-sample", type=int, default=1,
+                    help="vectors per part in each step of the reference (CPU oracle) arm")
+    return ap.parse_args(argv)
+
+
+# ---- distributed helpers (also exercised on CPU with gloo by the tests) ------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, local, world
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Rank 0 draws the specified states; other ranks draw their own batch."""
+    return base if rank == 0 else base + 1000 * rank
+
+
+def dist_max(value: float, device=None) -> float:
+    """Maximum of a float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---- clocks during the timed region ------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(1.0)  # let the sampler start before the timed region
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def mark(self):
+        return len(self.lines)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, first: int, last: int):
+        rows = []
+        for line in self.lines[first:last]:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        reasons = set()
+        for _, _, flags in rows:
+            for name, flag in zip(self.REASONS, flags[1:]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---- roofline inputs ---------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: torch copy, burst)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 copy measurement)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "walsh_hadamard_transform_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key: str):
+    """DRAM bytes per launch of `kernel_key` from the committed ncu summary, or None
+    when there is none or the kernel sources changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    rec = d.get(kernel_key)
+    if not rec or rec.get("source_sha") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---- our CUDA path ---------------------------------------------------------------
+
+def pass_names(w, fwt):
+    f = fwt.plan_factors(w.n, w.dtype)
+    names = []
+    for i, k in enumerate(f):
+        kind = "single" if len(f) == 1 else ("row" if i == 0 else "col")
+        names.append(f"{w.dtype} {kind} pass K={k} (n={w.n})")
+    return names
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import walsh_hadamard_transform_gb300 as fwt
+    from walsh_hadamard_transform_gb300 import inputs
+
+    rank, local, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    fwt.library()
+
+    parts = [inputs.WORKLOADS[name] for name in STEP_WORKLOADS[args.workload]]
+    host, dev_in, dev_out = [], [], []
+    for w in parts:
+        re, im = inputs.draw(w.values, w.n, w.batch, rank_seed(w.seed, rank), w.dtype)
+        host.append((re, im))
+        dev_in.append((torch.from_numpy(re).to(device), torch.from_numpy(im).to(device)))
+        dev_out.append((torch.empty_like(dev_in[-1][0]), torch.empty_like(dev_in[-1][1])))
+    torch.cuda.synchronize(device)
+
+    def step():
+        for w, (a, b), (c, d) in zip(parts, dev_in, dev_out):
+            fwt.transform(a, b, c, d, normalize=w.normalize)
+
+    names = [nm for w in parts for nm in pass_names(w, fwt)]
+    launches_per_step = len(names)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+
+    uuid = str(torch.cuda.get_device_properties(device).uuid)
+    sampler = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    sampler.start()
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * launches_per_step * args.steps)]
+    trace = fwt.PassTrace(events)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    mark0 = sampler.mark()
+    with trace:
+        t0.record()
+        for _ in range(args.steps):
+            step()
+        t1.record()
+    torch.cuda.synchronize(device)
+    barrier(device)
+    mark1 = sampler.mark()
+    elapsed_ms = t0.elapsed_time(t1)
+    elapsed_ms = dist_max(elapsed_ms, device)
+    sampler.stop()
+    clocks = sampler.summary(mark0, mark1)
+
+    durs = trace.durations_ms()
+    assert len(durs) == launches_per_step * args.steps, "pass trace incomplete"
+    per_kernel = {}
+    for i, d in enumerate(durs):
+        per_kernel.setdefault(i % launches_per_step, []).append(d)
+
+    vectors_per_rank = sum(w.batch for w in parts)
+    total_vectors = vectors_per_rank * world * args.steps
+    value = total_vectors / (elapsed_ms / 1e3)
+    algo_bytes_step = sum(2 * w.bytes_in for w in parts)  # 1 read + 1 write of every vector
+    peak, peak_src = measured_peaks()
+
+    # dominant kernel: largest share of device time
+    kernels = []
+    li = 0
+    for w in parts:
+        for nm in pass_names(w, fwt):
+            mean_ms = statistics.mean(per_kernel[li])
+            algo = 2 * w.bytes_in  # every pass reads and writes the whole batch once
+            kernels.append({"kernel": nm, "mean_ms": mean_ms, "total_ms": sum(per_kernel[li]),
+                            "algo_bytes_per_launch": algo, "gbs": algo / (mean_ms * 1e-3) / 1e9})
+            li += 1
+    top = max(kernels, key=lambda k: k["total_ms"])
+    traffic = ncu_traffic(top["kernel"])
+    roofline = {"bound": "hbm", "achieved": round(top["gbs"], 1), "peak": peak, "unit": "GB/s",
+                "frac": round(top["gbs"] / peak, 4), "traffic": traffic,
+                "kernel": top["kernel"], "peak_source": peak_src,
+                "algo_bytes_per_launch": top["algo_bytes_per_launch"]}
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "+".join(sorted({{"c64": "int64", "c32": "f32", "i32": "int32"}[w.dtype] for w in parts})),
+        "data": "synthetic (seeded PCG64; Gaussian unit-L2 states / uniform ints, per the workload)",
+        "config": {
+            "workload": args.workload,
+            "parts": [{"name": w.name, "n": w.n, "batch": w.batch, "dtype": w.dtype,
+                       "normalize": w.normalize, "factors": fwt.plan_factors(w.n, w.dtype)}
+                      for w in parts],
+            "layout": "split re/im arrays, batch-major, out of place",
+            "l2": "inputs larger than L2 (%.1f GiB in per step), no flush" % (
+                sum(w.bytes_in for w in parts) / 2 ** 30),
+            "arith": {"c64": "exact int64 fixed-point butterflies, one fp64 rounding per pass",
+                      "c32": "fp32", "i32": "int32 wrap"},
+        },
+        # algorithmic bytes (one read + one write of every vector) over the step time
+        "hbm_gbs_effective_per_gpu": round(algo_bytes_step * args.steps / (elapsed_ms / 1e3) / 1e9, 1),
+        "kernels": [{k: (round(v, 4) if isinstance(v, float) else v) for k, v in kk.items()} for kk in kernels],
+        "roofline": roofline,
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, parts, host, device, fwt, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(parts, host, args.cpu_sample)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def run_e2e(args, parts, host, device, fwt, world):
+    """Same metric through the public API with HOST buffers: every step copies its
+    inputs in from pinned memory, transforms, and copies the results back."""
+    import torch
+
+    pin_in, pin_out, work_in, work_out = [], [], [], []
+    for (re, im) in host:
+        a = torch.from_numpy(re).pin_memory()
+        b = torch.from_numpy(im).pin_memory()
+        pin_in.append((a, b))
+        pin_out.append((torch.empty_like(a).pin_memory(), torch.empty_like(b).pin_memory()))
+        work_in.append((torch.empty(a.shape, dtype=a.dtype, device=device),
+                        torch.empty(b.shape, dtype=b.dtype, device=device)))
+        work_out.append((torch.empty_like(work_in[-1][0]), torch.empty_like(work_in[-1][1])))
+    h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in pin_in)
+
+    def step():
+        for w, (a, b), (da, db), (oa, ob), (ha, hb) in zip(parts, pin_in, work_in, work_out, pin_out):
+            da.copy_(a, non_blocking=True)
+            db.copy_(b, non_blocking=True)
+            fwt.transform(da, db, oa, ob, normalize=w.normalize)
+            ha.copy_(oa, non_blocking=True)
+            hb.copy_(ob, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    t0.record()
+    for _ in range(args.e2e_steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize(device)
+    barrier(device)
+    ms = dist_max(t0.elapsed_time(t1), device)
+    vectors = sum(w.batch for w in parts) * world * args.e2e_steps
+    return {"value": round(vectors / (ms / 1e3), 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": h2d, "steps": args.e2e_steps,
+            "ms_per_step": round(ms / args.e2e_steps, 3)}
+
+
+def oracle_step(orc, parts, host, threads):
+    """Every real array of every part through the CPU oracle, the arrays run
+    concurrently (ctypes releases the GIL) and each split over whole vectors."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    jobs = [(arr, w.normalize) for w, pair in zip(parts, host) for arr in pair]
+    per_job = max(1, threads // len(jobs))
+    with ThreadPoolExecutor(max_workers=len(jobs)) as pool:
+        list(pool.map(lambda j: orc.fwt(j[0], normalize=j[1], nthreads=per_job), jobs))
+    return min(threads, sum(min(per_job, arr.shape[0]) for arr, _ in jobs))
+
+
+def cpu_baseline(parts, host, sample):
+    """The CPU oracle as it stands, on the first `sample` vectors of each part."""
+    import oracle
+
+    orc = oracle.default()
+    threads = max(1, os.cpu_count() or 1)
+    cut = [(re[:sample], im[:sample]) for re, im in host]
+    t = time.perf_counter()
+    used = oracle_step(orc, parts, cut, threads)
+    secs = time.perf_counter() - t
+    vectors = sum(min(sample, w.batch) for w in parts)
+    return {"value": round(vectors / secs, 4), "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": "first %d vectors of each part (%s), %.1f s wall on %d threads" % (
+                sample, ", ".join(w.name for w in parts), secs, used)}
+
+
+# ---- the reference arm: the CPU oracle -------------------------------------------------
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return  # rank 0 alone runs the CPU reference
+    import oracle
+    from walsh_hadamard_transform_gb300 import inputs
+
+    parts = [inputs.WORKLOADS[name] for name in STEP_WORKLOADS[args.workload]]
+    sample = max(1, min(args.ref_sample, min(w.batch for w in parts)))
+    host = [w.generate(batch=sample) for w in parts]
+    threads = max(1, os.cpu_count() or 1)
+    orc = oracle.default()
+    for _ in range(args.warmup):
+        oracle_step(orc, parts, host, threads)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        used = oracle_step(orc, parts, host, threads)
+    secs = time.perf_counter() - t
+    vectors = sample * len(parts) * args.steps
+    value = vectors / secs
+    desc = "first %d vectors of each part (%s) per step" % (sample, ", ".join(w.name for w in parts))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64+uint32 (oracle)",
+        "data": "synthetic (seeded PCG64)",
+        "config": {"workload": args.workload, "sample": desc},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": used, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.steps < 1 or args.warmup < 0:
+        raise SystemExit("--steps must be >= 1 and --warmup >= 0")
+    if args.impl == "reference":
+        # fewer, bounded CPU steps: each is seconds of host work
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

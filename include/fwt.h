@@ -1,0 +1,148 @@
+/*
+ * fwt.h -- batched Walsh-Hadamard transform on GB300 (sm_103a), C ABI.
+ *
+ * Operation (every entry point below):
+ *
+ *     y[k] = s * sum_{i=0}^{2^n - 1} (-1)^{popc(k & i)} x[i],   k = 0 .. 2^n - 1
+ *
+ * applied independently to each of `batch` vectors of 2^n amplitudes.  The sign
+ * rule is the natural-order (Sylvester) Hadamard matrix stated in
+ * "[QDP] [feature] Pr4 kronecker fwt", section "How" (the on-the-fly Hadamard
+ * value popc(k & i) of the naive GEMM placeholder).  s = 2^{-n/2} when
+ * `normalize` is non-zero, else 1.  The complex state is held as split real and
+ * imaginary arrays (the d_temp_real / d_temp_imag split of the same page); H is
+ * real, so each part is transformed on its own.
+ *
+ * Layout: batch-major and contiguous.  Vector b of each array occupies elements
+ * [b * 2^n, (b + 1) * 2^n).  Each array holds batch * 2^n elements.
+ *
+ * Memory and ownership: every pointer is a DEVICE pointer owned by the caller.
+ * The library allocates nothing, copies nothing to the host and never
+ * synchronises: the work is enqueued on `stream` (NULL = the legacy default
+ * stream of the current device) and the call returns at once.  Results are
+ * valid after the caller synchronises with `stream`.  Pointers must be 16-byte
+ * aligned (every cudaMalloc / PyTorch allocation is).
+ *
+ * In-place: re_out == re_in and/or im_out == im_in (exactly) is allowed.  Any
+ * other overlap between an output array and any array is rejected.
+ *
+ * Errors are returned synchronously.  Argument errors (INVALID_ARG, MISALIGNED,
+ * UNSUPPORTED) are detected before anything is launched, so such a call has
+ * enqueued no work.  FWT_ERR_CUDA means a CUDA call or launch failed;
+ * fwt_last_cuda_error() returns its cudaError_t.  A multi-pass transform may
+ * then have enqueued its earlier passes, and the output arrays are undefined.
+ * Faults that happen later on the device surface at the caller's
+ * synchronisation with `stream`.
+ *
+ * Thread safety: calls may be made from several host threads and devices; the
+ * per-device set-up (kernel attributes) is done once under a lock.
+ */
+#ifndef FWT_GB300_H
+#define FWT_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (struct CUstream_st *); NULL is the default stream. */
+typedef struct CUstream_st* fwt_stream_t;
+
+enum fwt_status {
+  FWT_OK = 0,
+  FWT_ERR_INVALID_ARG = 1, /* bad n / batch / null pointer / overlapping arrays */
+  FWT_ERR_MISALIGNED = 2,  /* a pointer is not 16-byte aligned */
+  FWT_ERR_UNSUPPORTED = 3, /* e.g. normalize with int32, or a plan the build lacks */
+  FWT_ERR_CUDA = 4,        /* a CUDA call failed; see fwt_last_cuda_error() */
+  FWT_ERR_TIMEOUT = 5      /* reserved: a bounded device wait gave up */
+};
+
+enum fwt_dtype { FWT_C32 = 0, FWT_C64 = 1, FWT_I32 = 2 };
+
+/*
+ * Complex fp32, split re/im.  0 <= n <= 30, batch >= 0 (batch == 0 is a no-op
+ * and accepts NULL pointers).  All four pointers must be non-NULL for batch > 0.
+ * Arithmetic is fp32 add/sub; the relative L2 error per vector is within
+ * n * 2^-24 of the exact transform of the input.
+ */
+int fwt_batched_c32(const float* re_in, const float* im_in, float* re_out, float* im_out,
+                    int n, int64_t batch, int normalize, fwt_stream_t stream);
+
+/*
+ * Complex fp64, split re/im.  Same arguments as fwt_batched_c32.  The butterflies
+ * run exactly in 64-bit fixed point on the integer units (one shared binary
+ * exponent per on-chip tile), with a single rounding back to fp64 per pass; the
+ * relative L2 error per vector stays below 1e-12 for finite input.  A tile that
+ * holds an Inf or NaN is transformed in plain IEEE fp64 instead, so Inf/NaN
+ * propagate as in IEEE arithmetic.
+ */
+int fwt_batched_c64(const double* re_in, const double* im_in, double* re_out, double* im_out,
+                    int n, int64_t batch, int normalize, fwt_stream_t stream);
+
+/*
+ * Exact int32 variant: add/sub modulo 2^32 (two's complement wrap), bit-exact.
+ * normalize must be 0 (2^{-n/2} is not an integer): FWT_ERR_UNSUPPORTED otherwise.
+ * Real-only input: pass im_in == im_out == NULL (both, or neither).
+ */
+int fwt_batched_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out,
+                    int32_t* im_out, int n, int64_t batch, int normalize, fwt_stream_t stream);
+
+/* Static text for a status code (never NULL). */
+const char* fwt_status_string(int status);
+
+/* cudaError_t (as int) of the most recent FWT_ERR_CUDA on this host thread, else 0. */
+int fwt_last_cuda_error(void);
+
+/*
+ * Number of HBM passes (one full read + write of the data each) the transform of
+ * a 2^n vector of `dtype` takes with the current plan: 1 while a vector fits one
+ * on-chip tile, 2 or 3 for the Kronecker split H_n = H_a (x) H_b (x) ...
+ * ("[QDP] [feature] Pr4 kronecker fwt", section "Why": H_n = H_{n/2} (x) H_{n/2};
+ * iThome "Day 18" FWT post, section "Kronecker block GEMM idea": H_N = H_a (x) H_b).
+ * Returns -1 for an invalid n or dtype.
+ */
+int fwt_plan_passes(int n, int dtype);
+
+/*
+ * Writes the factor sizes of the plan for (n, dtype), lowest index bits first,
+ * into bits[0 .. max_factors-1] and returns the number of factors (passes), or
+ * -1 for invalid input.  The factors sum to n.
+ */
+int fwt_plan_factors(int n, int dtype, int* bits, int max_factors);
+
+/*
+ * Tuning / testing: replace the plan for (n, dtype) by the given Kronecker
+ * factors (low bits first; nfactors in 1..3; each factor must be supported by a
+ * compiled tile shape, else FWT_ERR_UNSUPPORTED).  nfactors == 0 restores the
+ * default plan.  Applies process-wide to calls issued after it returns.
+ */
+int fwt_set_plan(int n, int dtype, int nfactors, const int* bits);
+
+/*
+ * Per-pass tracing with caller-owned CUDA events (tracing without a profiler).
+ * fwt_trace_events(events, capacity) arms tracing for the calling host thread:
+ * every pass launched afterwards by this thread is bracketed by two
+ * cudaEventRecord calls on the launch stream, into events[2i] and events[2i+1]
+ * (events are cudaEvent_t handles created by the caller, with timing enabled),
+ * until `capacity` events are used.  capacity == 0 disarms.  fwt_trace_count()
+ * returns how many events have been recorded since arming.  The library creates,
+ * destroys and synchronises nothing.  Returns FWT_OK or FWT_ERR_INVALID_ARG.
+ */
+int fwt_trace_events(void** events, int capacity);
+int fwt_trace_count(void);
+
+/*
+ * Host-only self-check of every compiled tile shape: runs the kernels' index
+ * maps on the CPU and verifies that each pass touches every element of its tile
+ * exactly once, transforms every index bit of its factor exactly once, and that
+ * every shared-memory access pattern is free of bank conflicts.  Returns 0 when
+ * all shapes pass, else the number of failures (details to stderr).  Needs no GPU.
+ */
+int fwt_selfcheck(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FWT_GB300_H */

@@ -1,0 +1,116 @@
+"""The C-ABI library: builds, exports every declared symbol, validates arguments
+on the host before any CUDA call, and its tile shapes pass the host self-check.
+CPU only: no call here reaches the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import walsh_hadamard_transform_gb300 as fwt
+from walsh_hadamard_transform_gb300 import build as fbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fwt.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fbuild.build()
+    return fwt.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fwt_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("fwt_batched_c32", "fwt_batched_c64", "fwt_batched_i32", "fwt_status_string",
+                 "fwt_plan_passes"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/fwt.h but not exported"
+
+
+def test_status_strings(lib):
+    for st in range(6):
+        assert fwt.status_string(st)
+    assert fwt.status_string(99) == "unknown status"
+
+
+def test_selfcheck_of_all_tile_shapes(lib):
+    assert fwt.selfcheck() == 0
+
+
+A = 0x10000  # fake, 16-byte aligned host addresses; validation never dereferences them
+GiB = 1 << 30
+
+
+@pytest.mark.parametrize("fn", ["fwt_batched_c32", "fwt_batched_c64", "fwt_batched_i32"])
+def test_argument_errors_return_before_launch(lib, fn):
+    f = getattr(fwt, fn)
+    norm = 0 if fn.endswith("i32") else 1
+    a, b, c, d = A, A + GiB, A + 2 * GiB, A + 3 * GiB
+    assert f(a, b, c, d, -1, 1, norm, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, c, d, 31, 1, norm, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, c, d, 4, -1, norm, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(None, None, None, None, 4, 0, norm, None) == fwt.FWT_OK  # empty batch
+    assert f(None, b, c, d, 4, 1, norm, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, None, d, 4, 1, norm, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, c, None, 4, 1, norm, None) == fwt.FWT_ERR_INVALID_ARG  # im half missing
+    assert f(a + 4, b, c, d, 4, 1, norm, None) == fwt.FWT_ERR_MISALIGNED
+    assert f(a, b, c, d + 8, 4, 1, norm, None) == fwt.FWT_ERR_MISALIGNED
+    # outputs overlapping anything other than their own input exactly
+    assert f(a, b, a + 16, d, 4, 1, norm, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, c, c, 4, 1, norm, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, b, d, 4, 1, norm, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, c, a, 4, 1, norm, None) == fwt.FWT_ERR_INVALID_ARG
+    # size overflow
+    assert f(a, b, c, d, 30, 1 << 40, norm, None) == fwt.FWT_ERR_INVALID_ARG
+
+
+def test_int32_rules(lib):
+    a, c = A, A + 2 * GiB
+    assert fwt.fwt_batched_i32(a, None, c, None, 4, 1, 1, None) == fwt.FWT_ERR_UNSUPPORTED
+    assert fwt.fwt_batched_c32(a, None, c, None, 4, 1, 1, None) == fwt.FWT_ERR_INVALID_ARG
+    assert fwt.fwt_batched_c64(a, None, c, None, 4, 1, 0, None) == fwt.FWT_ERR_INVALID_ARG
+
+
+def test_plans(lib):
+    for dt, rmax in (("c32", 15), ("c64", 14), ("i32", 15)):
+        for n in range(0, 31):
+            f = fwt.plan_factors(n, dt)
+            assert sum(f) == n and 1 <= len(f) <= 3
+            assert fwt.plan_passes(n, dt) == len(f)
+            assert (len(f) == 1) == (n <= rmax)
+    assert fwt.plan_factors(24, "c32") == [14, 10]
+    assert fwt.plan_factors(24, "c64") == [14, 10]
+    assert lib.fwt_plan_passes(31, 0) == -1 and lib.fwt_plan_passes(10, 7) == -1
+
+
+def test_plan_override_roundtrip(lib):
+    default = fwt.plan_factors(20, "c32")
+    fwt.set_plan(20, "c32", [10, 5, 5])
+    try:
+        assert fwt.plan_factors(20, "c32") == [10, 5, 5]
+        assert fwt.plan_passes(20, "c32") == 3
+    finally:
+        fwt.set_plan(20, "c32", None)
+    assert fwt.plan_factors(20, "c32") == default
+    for bad in ([10, 9], [16, 4], [2, 18], [4, 6, 10], [10, 11]):
+        with pytest.raises(fwt.FwtError):
+            fwt.set_plan(20, "c32", bad)
+    assert fwt.plan_factors(20, "c32") == default
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(fwt, "_lib", None)
+    monkeypatch.setattr(fwt, "LIBRARY", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        fwt.library()

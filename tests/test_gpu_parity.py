@@ -1,0 +1,249 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI (GPU only).
+
+Tolerances: int32 bit-exact; fp32 and fp64 per-vector complex relative L2 error
+<= 2e-6 and <= 1e-12 respectively (the transform's specification).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import walsh_hadamard_transform_gb300 as fwt
+from helpers import NP_DTYPE, TOL, assert_matches, gpu_transform, host_threads, rel_err_per_vector
+from walsh_hadamard_transform_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def need_cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    fwt.library()
+
+
+def _check(dtype, n, batch, normalize, seed, inplace=False, real_only=False):
+    re, im = inputs.random_pair(n, batch, dtype, seed)
+    if real_only:
+        im = None
+    gre, gim = gpu_transform(re, im, normalize, inplace=inplace)
+    ore, oim = oracle.fwt_complex(re, im, normalize=normalize, nthreads=host_threads())
+    assert_matches(dtype, gre, gim, ore, oim, f"{dtype} n={n} batch={batch} norm={normalize}")
+
+
+@pytest.mark.parametrize("dtype", ["c32", "c64", "i32"])
+@pytest.mark.parametrize("n", list(range(0, 21)))
+def test_every_n_small_batch(dtype, n):
+    # batch 3: several tiles and a ragged last tile wherever tiles pack short vectors
+    for normalize in ((False,) if dtype == "i32" else (True, False)):
+        _check(dtype, n, 3, normalize, seed=100 + n)
+
+
+@pytest.mark.parametrize("dtype", ["c32", "c64", "i32"])
+@pytest.mark.parametrize("n", [1, 7, 12, 15, 18, 22])
+def test_in_place(dtype, n):
+    _check(dtype, n, 2, dtype != "i32", seed=7 * n, inplace=True)
+
+
+@pytest.mark.parametrize("n", [5, 14, 19])
+def test_int32_real_only(n):
+    _check("i32", n, 4, False, seed=n, real_only=True)
+
+
+def _valid_plans(n, dtype):
+    out = []
+    for b in range(3, 16):
+        for rest in ([n - b], *[[a2, n - b - a2] for a2 in range(3, 11)]):
+            f = [b, *rest]
+            if any(k <= 0 for k in f):
+                continue
+            try:
+                fwt.set_plan(n, dtype, f)
+            except fwt.FwtError:
+                continue
+            out.append(f)
+    fwt.set_plan(n, dtype, None)
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["c32", "c64", "i32"])
+@pytest.mark.parametrize("n", [16, 20, 21])
+def test_every_kronecker_split(dtype, n):
+    """Each valid 2- and 3-factor split (every row and column tile shape) matches."""
+    plans = _valid_plans(n, dtype)
+    assert plans, "no valid plan"
+    re, im = inputs.random_pair(n, 2, dtype, seed=n)
+    norm = dtype != "i32"
+    ore, oim = oracle.fwt_complex(re, im, normalize=norm)
+    try:
+        for f in plans:
+            fwt.set_plan(n, dtype, f)
+            gre, gim = gpu_transform(re, im, norm)
+            assert_matches(dtype, gre, gim, ore, oim, f"plan {f}")
+    finally:
+        fwt.set_plan(n, dtype, None)
+
+
+@pytest.mark.parametrize("name", ["n10_b64_c32", "n12_b64_c32", "n14_b64_c32", "n18_b256_i32"])
+def test_workload_full_size(name):
+    w = inputs.WORKLOADS[name]
+    re, im = w.generate()
+    gre, gim = gpu_transform(re, im, w.normalize)
+    ore, oim = oracle.fwt_complex(re, im, normalize=w.normalize, nthreads=host_threads())
+    assert_matches(w.dtype, gre, gim, ore, oim, name)
+    if w.dtype == "i32":
+        assert np.abs(gre).max() <= 8 << 18  # no overflow at this size
+
+
+@pytest.mark.parametrize("name", ["n24_b16_c64", "n24_b16_c32"])
+def test_workload_n24_full_batch(name):
+    """Full batch on the GPU (the benchmarked call); the oracle checks two whole
+    vectors and sampled entries of every vector from the definition."""
+    w = inputs.WORKLOADS[name]
+    re, im = w.generate()
+    gre, gim = gpu_transform(re, im, w.normalize)
+    full = [0, w.batch - 1]
+    ore, oim = oracle.fwt_complex(re[full], im[full], normalize=True, nthreads=2)
+    assert_matches(w.dtype, gre[full], gim[full], ore, oim, name + " whole vectors")
+    rng = np.random.default_rng(0)
+    ks = np.concatenate([[0, 1, w.N - 1], rng.integers(0, w.N, size=5)])
+    for b in range(w.batch):
+        sre = oracle.entries(re[b], ks, normalize=True)
+        sim = oracle.entries(im[b], ks, normalize=True)
+        err = rel_err_per_vector(gre[b, ks], gim[b, ks], sre, sim)
+        assert err <= TOL[w.dtype], f"{name} vector {b}: sampled error {err:.3e}"
+    # Parseval on every vector (unit-norm inputs stay unit-norm)
+    norms = np.sqrt(np.sum(gre.astype(np.float64) ** 2 + gim.astype(np.float64) ** 2, axis=1))
+    assert np.allclose(norms, 1.0, rtol=0, atol=4 * TOL[w.dtype])
+
+
+def test_zero_batch_and_misaligned_on_device():
+    x = torch.zeros(2, 64, device="cuda")
+    y = torch.empty_like(x)
+    assert fwt.fwt_batched_c32(x.data_ptr(), x.data_ptr(), y.data_ptr(), y.data_ptr(), 6, 0, 1,
+                               None) == fwt.FWT_OK
+    big = torch.zeros(4096, device="cuda")
+    st = fwt.fwt_batched_c32(big.data_ptr() + 4, big[2048:].data_ptr(), y.data_ptr(),
+                             y[1].data_ptr(), 5, 1, 1, None)
+    assert st == fwt.FWT_ERR_MISALIGNED
+
+
+def test_guard_bands_untouched():
+    """Arrays embedded in larger buffers: nothing outside them is written."""
+    for dtype, n, batch in (("c32", 13, 3), ("c32", 20, 2), ("c64", 22, 1), ("i32", 9, 5)):
+        N = 1 << n
+        pad = 4096
+        re, im = inputs.random_pair(n, batch, dtype, seed=n)
+        t = {"c32": torch.float32, "c64": torch.float64, "i32": torch.int32}[dtype]
+        bufs = []
+        for src in (re, im):
+            b = torch.full((batch * N + 2 * pad,), 7, dtype=t, device="cuda")
+            b[pad:pad + batch * N] = torch.from_numpy(src.reshape(-1)).cuda()
+            bufs.append(b)
+        outs = [torch.full_like(b, 9) for b in bufs]
+        views = [b[pad:pad + batch * N].view(batch, N) for b in bufs + outs]
+        fwt.transform(views[0], views[1], views[2], views[3], normalize=dtype != "i32")
+        torch.cuda.synchronize()
+        for b, fill in ((bufs[0], 7), (bufs[1], 7), (outs[0], 9), (outs[1], 9)):
+            assert torch.all(b[:pad] == fill) and torch.all(b[-pad:] == fill), dtype
+        ore, oim = oracle.fwt_complex(re, im, normalize=dtype != "i32")
+        assert_matches(dtype, views[2].cpu().numpy(), views[3].cpu().numpy(), ore, oim, "guarded")
+
+
+def test_deterministic():
+    for dtype in ("c32", "c64"):
+        re, im = inputs.random_pair(21, 2, dtype, seed=5)
+        a = gpu_transform(re, im, True)
+        b = gpu_transform(re, im, True)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_nonfinite_values_propagate():
+    for dtype in ("c32", "c64"):
+        n = 16
+        re = np.zeros((2, 1 << n), NP_DTYPE[dtype])
+        im = np.zeros_like(re)
+        re[0, 5] = np.inf
+        re[1, 3] = np.inf
+        re[1, 6] = -np.inf
+        im[0, 9] = np.nan
+        gre, gim = gpu_transform(re, im, False)
+        ore, oim = oracle.fwt_complex(re, im, normalize=False)
+        for g, o in ((gre, ore), (gim, oim)):
+            assert np.array_equal(np.isnan(g), np.isnan(o)), dtype
+            fin = ~np.isnan(o)
+            assert np.array_equal(g[fin], o[fin].astype(g.dtype)), dtype
+
+
+def test_fp64_wide_dynamic_range():
+    """Entries from 1e-300 to 1e+300 (and subnormals) in one vector."""
+    rng = np.random.default_rng(3)
+    for n in (10, 14, 18, 24):
+        N = 1 << n
+        mags = 10.0 ** rng.uniform(-300, 300, size=(2, N))
+        re = (mags[0] * rng.choice([-1.0, 1.0], size=N))[None, :]
+        im = (mags[1] * rng.choice([-1.0, 1.0], size=N))[None, :]
+        re[0, : min(N, 64)] = 5e-324 * np.arange(min(N, 64))  # subnormals
+        for norm in (True, False):
+            gre, gim = gpu_transform(re, im, norm)
+            ore, oim = oracle.fwt_complex(re, im, normalize=norm, nthreads=2)
+            assert_matches("c64", gre, gim, ore, oim, f"dynamic range n={n} norm={norm}")
+
+
+def test_fp64_tiny_values_round_to_subnormals():
+    n = 12
+    re = np.full((1, 1 << n), 1e-310)
+    re[0, 1::2] = -3e-311
+    im = np.full_like(re, 2e-320)
+    gre, gim = gpu_transform(re, im, True)
+    ore, oim = oracle.fwt_complex(re, im, normalize=True)
+    assert_matches("c64", gre, gim, ore, oim, "subnormal outputs")
+
+
+@pytest.mark.parametrize("dtype", ["c32", "c64"])
+def test_odd_n_normalisation(dtype):
+    for n in (3, 11, 15, 17, 23, 25):
+        _check(dtype, n, 1, True, seed=n)
+
+
+def test_maximum_n_delta():
+    """n = 30 (2^30 amplitudes, 8 GiB of fp32 re+im, three passes), in place: a delta
+    at j gives s * (-1)^popc(k & j) everywhere; checked on sampled k."""
+    n = 30
+    N = 1 << n
+    j = 0x2AAAAAAB & (N - 1)
+    re = torch.zeros(1, N, device="cuda")
+    im = torch.zeros(1, N, device="cuda")
+    re[0, j] = 1.0
+    im[0, 0] = -2.0
+    fwt.transform(re, im, re, im, normalize=True)
+    torch.cuda.synchronize()
+    ks = torch.tensor(np.random.default_rng(1).integers(0, N, size=4096), device="cuda")
+    s = 2.0 ** (-n / 2)
+    par = torch.zeros_like(ks)
+    v = ks & j
+    while bool(v.any()):
+        par ^= v & 1
+        v = v >> 1
+    expect = s * (1.0 - 2.0 * par.double())
+    assert torch.allclose(re[0, ks].double(), expect, rtol=0, atol=1e-12)
+    assert torch.allclose(im[0, ks].double(), torch.full_like(expect, -2.0 * s), rtol=0, atol=1e-12)
+    total = float(re.double().pow(2).sum() + im.double().pow(2).sum())
+    assert abs(total - 5.0) < 1e-4
+    del re, im
+    torch.cuda.empty_cache()
+
+
+def test_involution_large():
+    """Normalised transform applied twice is the identity (fp32, fp64; n = 26, 3 passes)."""
+    for dtype, tol in (("c32", 4e-6), ("c64", 2e-12)):
+        re, im = inputs.random_pair(26, 1, dtype, seed=9)
+        t = torch.from_numpy(re).cuda(), torch.from_numpy(im).cuda()
+        a = fwt.transform(*t, normalize=True)
+        b = fwt.transform(*a, normalize=True)
+        torch.cuda.synchronize()
+        err = rel_err_per_vector(b[0].cpu().numpy(), b[1].cpu().numpy(), re, im)
+        assert err.max() < tol, dtype
+    x = torch.from_numpy(inputs.random_pair(26, 1, "i32", 1)[0]).cuda()
+    y = fwt.transform(x, None, normalize=False)[0]
+    z = fwt.transform(y, None, normalize=False)[0]
+    assert torch.equal(z, x << 26)

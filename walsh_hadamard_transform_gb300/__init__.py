@@ -1,0 +1,235 @@
+"""Batched Walsh-Hadamard transform on GB300 (sm_103a): Python binding.
+
+``y[k] = s * sum_i (-1)^popc(k & i) x[i]`` on batches of 2^n-amplitude complex
+vectors held as split real / imaginary arrays ("[QDP] [feature] Pr4 kronecker
+fwt", section "How"), with s = 2^{-n/2} when normalised.
+
+The functions named like the C ABI (``fwt_batched_c32`` ...) take raw device
+pointers and marshal arguments only; every step of the transform runs in the
+CUDA kernels of ``libfwt_gb300.so``.  ``transform`` is the tensor-level wrapper:
+it checks dtypes, devices and contiguity, then calls the C ABI on the current
+PyTorch stream.  There is no CPU fallback: without the compiled library (see
+``build.py``) every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_HERE, "libfwt_gb300.so")
+
+FWT_OK, FWT_ERR_INVALID_ARG, FWT_ERR_MISALIGNED = 0, 1, 2
+FWT_ERR_UNSUPPORTED, FWT_ERR_CUDA, FWT_ERR_TIMEOUT = 3, 4, 5
+FWT_C32, FWT_C64, FWT_I32 = 0, 1, 2
+DTYPES = {"c32": FWT_C32, "c64": FWT_C64, "i32": FWT_I32}
+
+
+class FwtError(RuntimeError):
+    """A non-zero status from the C ABI."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = f"{what}: {status_string(status)} ({status})"
+        if status == FWT_ERR_CUDA:
+            msg += f", cudaError {last_cuda_error()}"
+        super().__init__(msg)
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIBRARY):
+            raise RuntimeError(
+                f"{LIBRARY} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'` "
+                "(or python walsh_hadamard_transform_gb300/build.py)")
+        lib = ctypes.CDLL(LIBRARY)
+        vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        for name in ("fwt_batched_c32", "fwt_batched_c64", "fwt_batched_i32"):
+            f = getattr(lib, name)
+            f.argtypes = [vp, vp, vp, vp, ci, i64, ci, vp]
+            f.restype = ci
+        lib.fwt_status_string.argtypes = [ci]
+        lib.fwt_status_string.restype = ctypes.c_char_p
+        lib.fwt_last_cuda_error.argtypes = []
+        lib.fwt_last_cuda_error.restype = ci
+        lib.fwt_plan_passes.argtypes = [ci, ci]
+        lib.fwt_plan_passes.restype = ci
+        lib.fwt_plan_factors.argtypes = [ci, ci, ctypes.POINTER(ci), ci]
+        lib.fwt_plan_factors.restype = ci
+        lib.fwt_set_plan.argtypes = [ci, ci, ci, ctypes.POINTER(ci)]
+        lib.fwt_set_plan.restype = ci
+        lib.fwt_selfcheck.argtypes = []
+        lib.fwt_selfcheck.restype = ci
+        lib.fwt_trace_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ci]
+        lib.fwt_trace_events.restype = ci
+        lib.fwt_trace_count.argtypes = []
+        lib.fwt_trace_count.restype = ci
+        _lib = lib
+    return _lib
+
+
+# ---- C ABI, one Python function per entry point (argument marshalling only) -------
+
+def fwt_batched_c32(re_in, im_in, re_out, im_out, n, batch, normalize, stream) -> int:
+    return library().fwt_batched_c32(re_in, im_in, re_out, im_out, n, batch, int(normalize), stream)
+
+
+def fwt_batched_c64(re_in, im_in, re_out, im_out, n, batch, normalize, stream) -> int:
+    return library().fwt_batched_c64(re_in, im_in, re_out, im_out, n, batch, int(normalize), stream)
+
+
+def fwt_batched_i32(re_in, im_in, re_out, im_out, n, batch, normalize, stream) -> int:
+    return library().fwt_batched_i32(re_in, im_in, re_out, im_out, n, batch, int(normalize), stream)
+
+
+def status_string(status: int) -> str:
+    return library().fwt_status_string(int(status)).decode()
+
+
+def last_cuda_error() -> int:
+    return library().fwt_last_cuda_error()
+
+
+def plan_factors(n: int, dtype: str) -> list[int]:
+    buf = (ctypes.c_int * 3)()
+    k = library().fwt_plan_factors(int(n), DTYPES[dtype], buf, 3)
+    if k < 0:
+        raise ValueError(f"no plan for n={n} dtype={dtype}")
+    return list(buf)[:k]
+
+
+def plan_passes(n: int, dtype: str) -> int:
+    return library().fwt_plan_passes(int(n), DTYPES[dtype])
+
+
+def set_plan(n: int, dtype: str, factors) -> None:
+    """Override the Kronecker factors for (n, dtype); ``None`` or [] restores the default."""
+    factors = list(factors or [])
+    buf = (ctypes.c_int * max(1, len(factors)))(*factors)
+    st = library().fwt_set_plan(int(n), DTYPES[dtype], len(factors), buf)
+    if st != FWT_OK:
+        raise FwtError(st, f"fwt_set_plan(n={n}, {dtype}, {factors})")
+
+
+def selfcheck() -> int:
+    return library().fwt_selfcheck()
+
+
+class PassTrace:
+    """Record a CUDA event pair around every pass this thread launches.
+
+    ``events`` are ``torch.cuda.Event(enable_timing=True)`` objects (two per
+    traced pass).  Use as a context manager; ``durations_ms()`` afterwards gives
+    one device time per traced pass, in launch order."""
+
+    def __init__(self, events):
+        self.events = list(events)
+        for e in self.events:
+            e.record()  # makes torch create the underlying cudaEvent_t
+        self._handles = (ctypes.c_void_p * len(self.events))(*[e.cuda_event for e in self.events])
+        self.count = 0
+
+    def __enter__(self):
+        st = library().fwt_trace_events(self._handles, len(self.events))
+        if st != FWT_OK:
+            raise FwtError(st, "fwt_trace_events")
+        return self
+
+    def __exit__(self, *exc):
+        self.count = library().fwt_trace_count()
+        library().fwt_trace_events(None, 0)
+        return False
+
+    def durations_ms(self):
+        return [self.events[2 * i].elapsed_time(self.events[2 * i + 1])
+                for i in range(self.count // 2)]
+
+
+# ---- tensor-level wrapper ---------------------------------------------------------
+
+_ENTRY = {"c32": fwt_batched_c32, "c64": fwt_batched_c64, "i32": fwt_batched_i32}
+
+
+def _dtype_key(t) -> str:
+    import torch
+
+    key = {torch.float32: "c32", torch.float64: "c64", torch.int32: "i32"}.get(t.dtype)
+    if key is None:
+        raise TypeError(f"unsupported dtype {t.dtype}: use float32, float64 or int32")
+    return key
+
+
+def transform(re, im=None, out_re=None, out_im=None, normalize: bool = True, stream=None):
+    """Transform the rows of ``re`` / ``im`` (CUDA tensors of shape (batch, 2^n)).
+
+    Outputs are new tensors unless ``out_re`` / ``out_im`` are given (they may be
+    the inputs themselves, for an in-place transform).  ``im`` may be None only
+    for int32 (real-only input).  Runs on ``stream`` (default: the current
+    PyTorch stream); the call does not synchronise.  Returns (out_re, out_im).
+    """
+    import torch
+
+    key = _dtype_key(re)
+    if not re.is_cuda:
+        raise ValueError("transform() needs CUDA tensors; use transform_host() for host arrays")
+    if re.dim() != 2:
+        raise ValueError("expected a (batch, 2^n) tensor")
+    batch, N = re.shape
+    n = int(N).bit_length() - 1
+    if N < 1 or (1 << n) != N:
+        raise ValueError(f"row length {N} is not a power of two")
+    if out_re is None:
+        out_re = torch.empty_like(re)
+    if im is not None and out_im is None:
+        out_im = torch.empty_like(im)
+    for t in (re, im, out_re, out_im):
+        if t is None:
+            continue
+        if t.dtype != re.dtype or t.shape != re.shape or t.device != re.device:
+            raise ValueError("re, im and outputs must share dtype, shape and device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if stream is None:
+        stream = torch.cuda.current_stream(re.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(re.device):
+        st = _ENTRY[key](re.data_ptr(), im.data_ptr() if im is not None else None,
+                         out_re.data_ptr(), out_im.data_ptr() if out_im is not None else None,
+                         n, batch, normalize, handle)
+    if st != FWT_OK:
+        raise FwtError(st, f"fwt_batched_{key}(n={n}, batch={batch})")
+    return out_re, out_im
+
+
+def transform_host(re, im=None, normalize: bool = True, device="cuda", stream=None,
+                   work=None):
+    """End-to-end transform of HOST tensors: copy in, transform on the GPU, copy out.
+
+    ``re`` / ``im`` are CPU tensors (pinned memory gives asynchronous copies).
+    ``work`` may hold preallocated device tensors (re_dev, im_dev) to reuse.
+    Returns host tensors (the result is complete when this returns).
+    """
+    import torch
+
+    if work is None:
+        work = (torch.empty(re.shape, dtype=re.dtype, device=device),
+                None if im is None else torch.empty(im.shape, dtype=im.dtype, device=device))
+    dre, dim_ = work
+    dre.copy_(re, non_blocking=True)
+    if im is not None:
+        dim_.copy_(im, non_blocking=True)
+    transform(dre, dim_, dre, dim_, normalize=normalize, stream=stream)
+    hre = torch.empty(re.shape, dtype=re.dtype, pin_memory=re.is_pinned())
+    hre.copy_(dre, non_blocking=True)
+    him = None
+    if im is not None:
+        him = torch.empty(im.shape, dtype=im.dtype, pin_memory=im.is_pinned())
+        him.copy_(dim_, non_blocking=True)
+    torch.cuda.current_stream(dre.device).synchronize()
+    return hre, him

@@ -1,0 +1,320 @@
+// C ABI of the batched Walsh-Hadamard transform: argument checks, the pass
+// planner (Kronecker split of H_n into on-chip factors) and the launches.
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fwt.h"
+#include "registry.cuh"
+
+namespace fwt {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+// per-thread pass tracing into caller-owned events
+thread_local void** g_trace_events = nullptr;
+thread_local int g_trace_capacity = 0;
+thread_local int g_trace_count = 0;
+
+const std::vector<KernelEntry>& table() {
+  static const std::vector<KernelEntry> t = [] {
+    std::vector<KernelEntry> v;
+    register_c32(v);
+    register_c64(v);
+    register_i32(v);
+    return v;
+  }();
+  return t;
+}
+
+const KernelEntry* find_kernel(int dtype, int kind, int K) {
+  for (const KernelEntry& e : table())
+    if (e.dtype == dtype && e.kind == kind && e.K == K) return &e;
+  return nullptr;
+}
+
+int elem_size(int dtype) { return dtype == FWT_C64 ? 8 : 4; }
+int col_width_log(int dtype) { return dtype == FWT_C64 ? 4 : 5; }  // 128-byte column segments
+
+// ---- plans -----------------------------------------------------------------------
+// A plan is the list of Kronecker factors H_n = H_{f_last} (x) ... (x) H_{f_0}, each
+// an on-chip pass over f_i consecutive index bits, lowest bits first.  Factor 0 is
+// a row pass over contiguous memory, the others are column passes in place.
+struct Plan {
+  int nf = 0;
+  int bits[3] = {0, 0, 0};
+};
+
+std::mutex g_plan_mu;
+Plan g_override[3][31];  // nf == 0: no override
+
+int max_row_bits(int dtype) { return dtype == FWT_C64 ? 14 : 15; }
+int min_col_bits(int dtype) { return dtype == FWT_C64 ? 6 : 5; }
+int max_col_bits(int) { return 10; }
+
+bool plan_valid(int n, int dtype, const Plan& p) {
+  if (p.nf < 1 || p.nf > 3) return false;
+  int sum = 0;
+  for (int f = 0; f < p.nf; ++f) {
+    const int k = p.bits[f];
+    if (f == 0) {
+      if (k <= 2) {
+        if (p.nf != 1 || !find_kernel(dtype, KIND_SMALL, k)) return false;
+      } else if (!find_kernel(dtype, KIND_ROW, k)) {
+        return false;
+      }
+    } else {
+      if (!find_kernel(dtype, KIND_COL, k)) return false;
+      if (sum < col_width_log(dtype)) return false;  // a column segment must fit one row
+    }
+    sum += k;
+  }
+  return sum == n;
+}
+
+Plan default_plan(int n, int dtype) {
+  Plan p;
+  const int rmax = max_row_bits(dtype), cmin = min_col_bits(dtype), cmax = max_col_bits(dtype);
+  if (n <= rmax) {
+    p.nf = 1;
+    p.bits[0] = n;
+    return p;
+  }
+  const int row_pref = 14;  // 64 KiB (fp32) / 128 KiB (fp64) row tiles
+  if (n <= rmax + cmax) {
+    int a = std::min(std::max(cmin, n - row_pref), cmax);
+    if (n - a > rmax) a = n - rmax;
+    p.nf = 2;
+    p.bits[0] = n - a;
+    p.bits[1] = a;
+    return p;
+  }
+  // three factors: a row factor and two column factors of about equal size
+  const int b = std::min(row_pref, n - 2 * cmin);
+  const int rest = n - b;
+  p.nf = 3;
+  p.bits[0] = b;
+  p.bits[1] = (rest + 1) / 2;
+  p.bits[2] = rest / 2;
+  return p;
+}
+
+Plan get_plan(int n, int dtype) {
+  {
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    const Plan& o = g_override[dtype][n];
+    if (o.nf > 0) return o;
+  }
+  return default_plan(n, dtype);
+}
+
+// ---- per-device set-up -------------------------------------------------------------
+std::mutex g_dev_mu;
+std::vector<char> g_dev_ready;
+
+cudaError_t ensure_device() {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if ((int)g_dev_ready.size() <= dev) g_dev_ready.resize(dev + 1, 0);
+  if (g_dev_ready[dev]) return cudaSuccess;
+  for (const KernelEntry& e : table()) {
+    err = e.setup();
+    if (err != cudaSuccess) return err;
+  }
+  g_dev_ready[dev] = 1;
+  return cudaSuccess;
+}
+
+// floor(2^64 / sqrt(2)) = floor(sqrt(2^127)), by bitwise integer square root.
+unsigned long long rsqrt2_q64() {
+  const unsigned __int128 target = (unsigned __int128)1 << 127;
+  unsigned __int128 r = 0;
+  for (int bit = 63; bit >= 0; --bit) {
+    const unsigned __int128 c = r | ((unsigned __int128)1 << bit);
+    if (c * c <= target) r = c;
+  }
+  return (unsigned long long)r;
+}
+
+bool overlaps(const void* a, const void* b, size_t bytes) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + bytes && y < x + bytes;
+}
+
+int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out, int n,
+        int64_t batch, int normalize, cudaStream_t stream) {
+  if (n < 0 || n > 30 || batch < 0) return FWT_ERR_INVALID_ARG;
+  if (dtype == FWT_I32 && normalize) return FWT_ERR_UNSUPPORTED;
+  if (batch == 0) return FWT_OK;
+  const int esz = elem_size(dtype);
+  if (batch > (INT64_MAX >> n) / esz) return FWT_ERR_INVALID_ARG;
+  const long long comp_elems = (long long)batch << n;
+  const size_t bytes = (size_t)comp_elems * (size_t)esz;
+  // pointers: real part required; imaginary part both-or-neither (NULL only for int32)
+  if (!re_in || !re_out) return FWT_ERR_INVALID_ARG;
+  const bool has_im = im_in || im_out;
+  if (has_im && (!im_in || !im_out)) return FWT_ERR_INVALID_ARG;
+  if (!has_im && dtype != FWT_I32) return FWT_ERR_INVALID_ARG;
+  const void* ptrs[4] = {re_in, im_in, re_out, im_out};
+  for (const void* q : ptrs)
+    if (q && ((uintptr_t)q & 15u)) return FWT_ERR_MISALIGNED;
+  // outputs may coincide exactly with their own input, and with nothing else
+  if (overlaps(re_out, re_in, bytes) && re_out != re_in) return FWT_ERR_INVALID_ARG;
+  if (has_im) {
+    if (overlaps(im_out, im_in, bytes) && im_out != im_in) return FWT_ERR_INVALID_ARG;
+    if (overlaps(re_out, im_out, bytes) || overlaps(re_out, im_in, bytes) ||
+        overlaps(im_out, re_in, bytes))
+      return FWT_ERR_INVALID_ARG;
+  }
+  const Plan plan = get_plan(n, dtype);
+  if (!plan_valid(n, dtype, plan)) return FWT_ERR_UNSUPPORTED;
+
+  cudaError_t err = ensure_device();
+  if (err != cudaSuccess) {
+    g_last_cuda_error = (int)err;
+    return FWT_ERR_CUDA;
+  }
+
+  PassParams p{};
+  p.comp_elems = comp_elems;
+  const double s = n % 2 == 0 ? std::ldexp(1.0, -n / 2) : std::ldexp(1.0, -(n - 1) / 2) / std::sqrt(2.0);
+  p.scale_f64 = s;
+  p.scale_f32 = (float)s;
+  p.scale_exp = -(n / 2);
+  p.scale_half = n % 2;
+  p.rsqrt2_q64 = rsqrt2_q64();
+  const int ncomp = has_im ? 2 : 1;
+  int L = 0;
+  for (int f = 0; f < plan.nf; ++f) {
+    const int K = plan.bits[f];
+    const KernelEntry* e;
+    long long tiles;
+    if (f == 0 && K <= 2) {
+      e = find_kernel(dtype, KIND_SMALL, K);
+      tiles = ((comp_elems >> K) + 255) / 256;
+    } else if (f == 0) {
+      e = find_kernel(dtype, KIND_ROW, K);
+      tiles = (comp_elems + (1ll << e->TB) - 1) >> e->TB;
+    } else {
+      e = find_kernel(dtype, KIND_COL, K);
+      tiles = comp_elems >> e->TB;
+    }
+    if (tiles > INT_MAX) return FWT_ERR_UNSUPPORTED;
+    p.in[0] = f == 0 ? re_in : re_out;
+    p.in[1] = f == 0 ? im_in : im_out;
+    p.out[0] = re_out;
+    p.out[1] = im_out;
+    p.stride_log = L;
+    p.do_scale = (normalize && f == plan.nf - 1) ? 1 : 0;
+    const bool traced = g_trace_count + 2 <= g_trace_capacity;
+    if (traced) {
+      err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count], stream);
+      if (err != cudaSuccess) {
+        g_last_cuda_error = (int)err;
+        return FWT_ERR_CUDA;
+      }
+    }
+    err = e->launch(p, tiles, ncomp, stream);
+    if (err == cudaSuccess && traced) {
+      err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count + 1], stream);
+      g_trace_count += 2;
+    }
+    if (err != cudaSuccess) {
+      g_last_cuda_error = (int)err;
+      return FWT_ERR_CUDA;
+    }
+    L += K;
+  }
+  return FWT_OK;
+}
+
+}  // namespace
+}  // namespace fwt
+
+extern "C" {
+
+int fwt_batched_c32(const float* re_in, const float* im_in, float* re_out, float* im_out, int n,
+                    int64_t batch, int normalize, fwt_stream_t stream) {
+  return fwt::run(FWT_C32, re_in, im_in, re_out, im_out, n, batch, normalize, (cudaStream_t)stream);
+}
+
+int fwt_batched_c64(const double* re_in, const double* im_in, double* re_out, double* im_out,
+                    int n, int64_t batch, int normalize, fwt_stream_t stream) {
+  return fwt::run(FWT_C64, re_in, im_in, re_out, im_out, n, batch, normalize, (cudaStream_t)stream);
+}
+
+int fwt_batched_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, int32_t* im_out,
+                    int n, int64_t batch, int normalize, fwt_stream_t stream) {
+  return fwt::run(FWT_I32, re_in, im_in, re_out, im_out, n, batch, normalize, (cudaStream_t)stream);
+}
+
+const char* fwt_status_string(int status) {
+  switch (status) {
+    case FWT_OK: return "ok";
+    case FWT_ERR_INVALID_ARG: return "invalid argument";
+    case FWT_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case FWT_ERR_UNSUPPORTED: return "unsupported";
+    case FWT_ERR_CUDA: return "CUDA error";
+    case FWT_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int fwt_last_cuda_error(void) { return fwt::g_last_cuda_error; }
+
+int fwt_plan_factors(int n, int dtype, int* bits, int max_factors) {
+  if (n < 0 || n > 30 || dtype < 0 || dtype > 2) return -1;
+  const fwt::Plan p = fwt::get_plan(n, dtype);
+  for (int f = 0; f < p.nf && f < max_factors; ++f) bits[f] = p.bits[f];
+  return p.nf;
+}
+
+int fwt_plan_passes(int n, int dtype) { return fwt_plan_factors(n, dtype, nullptr, 0); }
+
+int fwt_set_plan(int n, int dtype, int nfactors, const int* bits) {
+  if (n < 0 || n > 30 || dtype < 0 || dtype > 2 || nfactors < 0 || nfactors > 3)
+    return FWT_ERR_INVALID_ARG;
+  fwt::Plan p;
+  p.nf = nfactors;
+  for (int f = 0; f < nfactors; ++f) {
+    if (!bits) return FWT_ERR_INVALID_ARG;
+    p.bits[f] = bits[f];
+  }
+  if (nfactors > 0 && !fwt::plan_valid(n, dtype, p)) return FWT_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
+  fwt::g_override[dtype][n] = p;
+  return FWT_OK;
+}
+
+int fwt_trace_events(void** events, int capacity) {
+  if (capacity < 0 || (capacity > 0 && !events)) return FWT_ERR_INVALID_ARG;
+  fwt::g_trace_events = capacity > 0 ? events : nullptr;
+  fwt::g_trace_capacity = capacity;
+  fwt::g_trace_count = 0;
+  return FWT_OK;
+}
+
+int fwt_trace_count(void) { return fwt::g_trace_count; }
+
+int fwt_selfcheck(void) {
+  int fails = 0;
+  for (const fwt::KernelEntry& e : fwt::table()) fails += e.selfcheck();
+  for (int dt = 0; dt < 3; ++dt)
+    for (int n = 0; n <= 30; ++n)
+      if (!fwt::plan_valid(n, dt, fwt::default_plan(n, dt))) {
+        fprintf(stderr, "fwt_selfcheck: no valid default plan for n=%d dtype=%d\n", n, dt);
+        ++fails;
+      }
+  return fails;
+}
+
+}  // extern "C"

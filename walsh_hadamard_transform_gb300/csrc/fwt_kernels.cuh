@@ -1,0 +1,320 @@
+// Pass kernels of the batched Walsh-Hadamard transform (sm_103a).
+//
+// One launch = one pass over every vector of the batch: a full HBM read and write
+// of the data.  A pass transforms a contiguous group of index bits of each 2^n
+// vector with the on-chip tile engine:
+//
+//   row tiles:    bits [0, K) of each vector; a tile is 2^TB contiguous elements
+//                 (one vector, one row of the Kronecker split, or several short
+//                 vectors).  This is the whole transform when n fits a tile, and
+//                 the I (x) H_b factor of the Kronecker split otherwise.
+//   column tiles: bits [L, L + K) of each vector; a tile is 2^K rows spaced 2^L
+//                 elements apart, times one 128-byte segment of contiguous
+//                 columns.  This is the H_a (x) I factor of the Kronecker split
+//                 ("[QDP] [feature] Pr4 kronecker fwt", section "Why submit PR4",
+//                 deliverables: Y = (H_{n1} (x) I)(I (x) H_{n2}) X; iThome "Day
+//                 18" FWT post, section "Kronecker block GEMM idea": Z = X H_b,
+//                 Y = H_a Z).  The strided tile is read and written in place, so
+//                 the transpose between the two factors happens in the loads and
+//                 stores and never as a separate pass or a temporary buffer.
+//
+// fp64 runs its butterflies exactly in 64-bit fixed point on the integer units
+// (GB300's fp64 add rate is about 1/64 of its fp32 rate, while 64-bit integer
+// adds run near the fp32 rate): the tile's largest binary exponent sets a common
+// scale, every element is converted to an int64 with 61 - K fraction bits of
+// headroom below it, the K stages run exactly, and each result is rounded once
+// back to fp64 (round to nearest even).  Both conversions use integer bit
+// arithmetic only.  A tile holding an Inf or NaN takes a plain fp64 path instead.
+#pragma once
+
+#include <cstdint>
+#include <type_traits>
+
+#include <cuda_runtime.h>
+
+#include "tile_engine.cuh"
+
+namespace fwt {
+
+struct PassParams {
+  const void* in[2];
+  void* out[2];
+  long long comp_elems;  // elements per array (batch * 2^n)
+  int stride_log;        // column tiles: log2 of the row stride L; row tiles: 0
+  int do_scale;          // apply the normalisation in this pass
+  float scale_f32;       // 2^{-n/2} rounded to fp32
+  double scale_f64;      // 2^{-n/2} in fp64
+  int scale_exp;         // fixed point: floor(-n/2) as a binary exponent
+  int scale_half;        // fixed point: n odd, also divide by sqrt(2)
+  unsigned long long rsqrt2_q64;  // floor(2^64 / sqrt(2))
+};
+
+// ---- arithmetic policies ----------------------------------------------------------
+struct ArithF32 {
+  __device__ static float add(float a, float b) { return a + b; }
+  __device__ static float sub(float a, float b) { return a - b; }
+};
+struct ArithU32 {  // two's complement wrap, bit-exact for int32 data
+  __device__ static uint32_t add(uint32_t a, uint32_t b) { return a + b; }
+  __device__ static uint32_t sub(uint32_t a, uint32_t b) { return a - b; }
+};
+struct ArithF64 {
+  __device__ static double add(double a, double b) { return a + b; }
+  __device__ static double sub(double a, double b) { return a - b; }
+};
+struct ArithI64 {  // magnitudes stay below 2^62 by construction; no wrap occurs
+  __device__ static long long add(long long a, long long b) {
+    return (long long)((unsigned long long)a + (unsigned long long)b);
+  }
+  __device__ static long long sub(long long a, long long b) {
+    return (long long)((unsigned long long)a - (unsigned long long)b);
+  }
+};
+
+// ---- global memory access -------------------------------------------------------
+template <typename U>
+__device__ __forceinline__ typename Vec16<U>::type ldg16(const void* p) {
+  using V = typename Vec16<U>::type;
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return *reinterpret_cast<V*>(&v);
+}
+template <typename U>
+__device__ __forceinline__ void stg16(void* p, const typename Vec16<U>::type& val) {
+  const uint4 v = *reinterpret_cast<const uint4*>(&val);
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Tile-local index -> element offset within the array.
+template <class S, bool COLS>
+struct TileMap {
+  long long base;
+  int L;
+  long long valid;  // row tiles: elements of this tile inside the array
+  __device__ __forceinline__ long long off(uint32_t u) const {
+    if constexpr (!COLS) {
+      return base + (long long)u;
+    } else {
+      constexpr int CWL = S::TS;  // column bits sit below the transformed rows
+      return base + ((long long)(u >> CWL) << L) + (long long)(u & ((1u << CWL) - 1u));
+    }
+  }
+  __device__ __forceinline__ bool in_range(uint32_t u) const {
+    if constexpr (!COLS && S::TB > S::TK) return (long long)u < valid;  // ragged last tile
+    else return true;
+  }
+  __device__ static TileMap make(const PassParams& p, long long tile) {
+    TileMap m;
+    m.L = p.stride_log;
+    if constexpr (!COLS) {
+      m.base = tile << S::TB;
+      m.valid = p.comp_elems - m.base;
+    } else {
+      const int chunks_lg = p.stride_log - S::TS;
+      const long long cc = tile & ((1ll << chunks_lg) - 1);
+      const long long hb = tile >> chunks_lg;
+      m.base = (hb << (p.stride_log + S::TK)) + (cc << S::TS);
+      m.valid = 0;
+    }
+    return m;
+  }
+};
+
+template <class S, bool COLS, typename T, typename U>
+__device__ __forceinline__ void load_tile(const T* in, const TileMap<S, COLS>& m, U (&x)[S::NE]) {
+  using V = typename Vec16<U>::type;
+  const uint32_t t = threadIdx.x;
+#pragma unroll
+  for (int j = 0; j < S::NV; ++j) {
+    const uint32_t u = S::idx1(t, j * S::VEC);
+    V v;
+    if (m.in_range(u)) v = ldg16<U>(in + m.off(u));
+    else v = V{};
+    const U* pv = reinterpret_cast<const U*>(&v);
+#pragma unroll
+    for (int i = 0; i < S::VEC; ++i) x[j * S::VEC + i] = pv[i];
+  }
+}
+
+template <class S, bool COLS, typename T, typename U>
+__device__ __forceinline__ void store_tile(T* out, const TileMap<S, COLS>& m, const U (&x)[S::NE]) {
+  using V = typename Vec16<U>::type;
+  const uint32_t t = threadIdx.x;
+#pragma unroll
+  for (int j = 0; j < S::NV; ++j) {
+    const uint32_t u = S::idx3(t, j * S::VEC);
+    V v;
+    U* pv = reinterpret_cast<U*>(&v);
+#pragma unroll
+    for (int i = 0; i < S::VEC; ++i) pv[i] = x[j * S::VEC + i];
+    if (m.in_range(u)) stg16<U>(out + m.off(u), v);
+  }
+}
+
+// ---- fp32 / int32 / plain fp64 tile ---------------------------------------------
+template <class S, class A, bool COLS, typename T>
+__device__ __forceinline__ void plain_tile(const PassParams& p, unsigned char* smem_raw) {
+  const bool im = blockIdx.y != 0;
+  const T* in = static_cast<const T*>(im ? p.in[1] : p.in[0]);
+  T* out = static_cast<T*>(im ? p.out[1] : p.out[0]);
+  const auto m = TileMap<S, COLS>::make(p, (long long)blockIdx.x);
+  T x[S::NE];
+  load_tile<S, COLS>(in, m, x);
+  tile_rounds<S, A>(x, reinterpret_cast<T*>(smem_raw));
+  if (p.do_scale) {
+    if constexpr (sizeof(T) == 4 && !std::is_integral<T>::value) {
+#pragma unroll
+      for (int r = 0; r < S::NE; ++r) x[r] = x[r] * p.scale_f32;
+    } else if constexpr (sizeof(T) == 8) {
+#pragma unroll
+      for (int r = 0; r < S::NE; ++r) x[r] = x[r] * p.scale_f64;
+    }
+  }
+  store_tile<S, COLS>(out, m, x);
+}
+
+// ---- fp64 in exact 64-bit fixed point -------------------------------------------
+// Biased exponent field used for scaling: subnormals and zeros count as 1.
+__device__ __forceinline__ uint32_t exp_key(long long bits) {
+  const uint32_t e = (uint32_t)((unsigned long long)bits >> 52) & 0x7ffu;
+  return e == 0x7ffu ? 0x800u : (e == 0 ? 1u : e);  // 0x800: Inf or NaN present
+}
+
+// q = round(v * 2^(F + 1023 - emax)) for |v| < 2^(emax - 1022): |q| <= 2^(F+1).
+__device__ __forceinline__ long long to_fixed(long long bits, int emax, int F) {
+  const unsigned long long b = (unsigned long long)bits;
+  const int e = (int)((b >> 52) & 0x7ffu);
+  const unsigned long long m =
+      (b & 0x000fffffffffffffull) | (e ? 0x0010000000000000ull : 0ull);
+  const int sh = (e ? e : 1) - emax + F - 52;
+  unsigned long long mag;
+  if (sh >= 0) {
+    mag = m << sh;
+  } else {
+    const int rs1 = min(-sh - 1, 63);  // shift by (rs - 1), then round half up
+    mag = ((m >> rs1) + 1ull) >> 1;
+  }
+  return (b >> 63) ? -(long long)mag : (long long)mag;
+}
+
+// Rounds q * 2^e0 (optionally also / sqrt 2) to the nearest fp64, ties to even.
+__device__ __forceinline__ long long from_fixed(long long q, int e0, int half,
+                                                unsigned long long rsqrt2) {
+  const unsigned long long sign = (unsigned long long)q & 0x8000000000000000ull;
+  unsigned long long a = q < 0 ? (unsigned long long)(-q) : (unsigned long long)q;
+  if (half) a = __umul64hi(a, rsqrt2);  // a / sqrt(2), truncated (error < 1 unit)
+  if (a == 0) return 0;
+  const int top = 63 - __clzll((long long)a);
+  int be = top + e0 + 1023;  // biased exponent of the result
+  if (be >= 1) {
+    unsigned long long mant;
+    if (top <= 52) {
+      mant = a << (52 - top);
+    } else {
+      const int rs = top - 52;
+      mant = a >> rs;
+      const unsigned long long rem = a & ((1ull << rs) - 1ull);
+      const unsigned long long halfulp = 1ull << (rs - 1);
+      mant += (rem > halfulp) || (rem == halfulp && (mant & 1ull));
+      if (mant >> 53) { mant >>= 1; ++be; }
+    }
+    if (be >= 2047) return (long long)(sign | 0x7ff0000000000000ull);  // overflow -> Inf
+    return (long long)(sign | ((unsigned long long)be << 52) | (mant & 0x000fffffffffffffull));
+  }
+  // subnormal result, in units of 2^-1074
+  const int rs = -(e0 + 1074);
+  if (rs <= 0) return (long long)(sign | (a << (-rs)));  // exact: fits in 52 bits when be < 1
+  if (rs >= 64) {
+    const bool up = rs == 64 && a > 0x8000000000000000ull;
+    return (long long)(sign | (up ? 1ull : 0ull));
+  }
+  unsigned long long t = a >> rs;
+  const unsigned long long rem = a & ((1ull << rs) - 1ull);
+  const unsigned long long halfulp = 1ull << (rs - 1);
+  t += (rem > halfulp) || (rem == halfulp && (t & 1ull));
+  return (long long)(sign | t);
+}
+
+template <class S, bool COLS>
+__device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* smem_raw) {
+  __shared__ uint32_t red[32];
+  const bool im = blockIdx.y != 0;
+  const double* in = static_cast<const double*>(im ? p.in[1] : p.in[0]);
+  double* out = static_cast<double*>(im ? p.out[1] : p.out[0]);
+  const auto m = TileMap<S, COLS>::make(p, (long long)blockIdx.x);
+  long long x[S::NE];
+  load_tile<S, COLS>(reinterpret_cast<const long long*>(in), m, x);
+  // tile-wide largest exponent (and whether any Inf/NaN is present)
+  uint32_t key = 1;
+#pragma unroll
+  for (int r = 0; r < S::NE; ++r) key = max(key, exp_key(x[r]));
+  key = __reduce_max_sync(0xffffffffu, key);
+  if ((threadIdx.x & 31u) == 0) red[threadIdx.x >> 5] = key;
+  __syncthreads();
+  key = red[0];
+#pragma unroll
+  for (int w = 1; w < S::NT / 32; ++w) key = max(key, red[w]);
+  if (key >= 0x800u) {  // IEEE path for tiles with Inf/NaN
+    double xd[S::NE];
+#pragma unroll
+    for (int r = 0; r < S::NE; ++r) xd[r] = __longlong_as_double(x[r]);
+    tile_rounds<S, ArithF64>(xd, reinterpret_cast<double*>(smem_raw));
+    if (p.do_scale) {
+#pragma unroll
+      for (int r = 0; r < S::NE; ++r) xd[r] = xd[r] * p.scale_f64;
+    }
+    store_tile<S, COLS>(out, m, xd);
+    return;
+  }
+  const int emax = (int)key;
+  constexpr int F = 61 - S::TK;  // headroom: |q| <= 2^(F+1) grows by 2^TK
+#pragma unroll
+  for (int r = 0; r < S::NE; ++r) x[r] = to_fixed(x[r], emax, F);
+  tile_rounds<S, ArithI64>(x, reinterpret_cast<long long*>(smem_raw));
+  const int e0 = emax - 1023 - F + (p.do_scale ? p.scale_exp : 0);
+  const int half = p.do_scale ? p.scale_half : 0;
+#pragma unroll
+  for (int r = 0; r < S::NE; ++r) x[r] = from_fixed(x[r], e0, half, p.rsqrt2_q64);
+  store_tile<S, COLS>(reinterpret_cast<long long*>(out), m, x);
+}
+
+// ---- kernels --------------------------------------------------------------------
+// KIND: 0 = fp32, 1 = fp64 (fixed point), 2 = int32, 3 = fp64 plain IEEE
+// Two CTAs per SM for tiles up to 256 threads (at most 128 registers a thread).
+template <class S, int KIND, bool COLS>
+__global__ void __launch_bounds__(S::NT, S::NT <= 256 ? 2 : 1) fwt_tile_kernel(const PassParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  if constexpr (KIND == 0) plain_tile<S, ArithF32, COLS, float>(p, smem_raw);
+  else if constexpr (KIND == 1) fixed_tile<S, COLS>(p, smem_raw);
+  else if constexpr (KIND == 2) plain_tile<S, ArithU32, COLS, uint32_t>(p, smem_raw);
+  else plain_tile<S, ArithF64, COLS, double>(p, smem_raw);
+}
+
+// Vectors of 2^NL <= 4 elements: one thread per vector, plain arithmetic.
+template <typename T, class A, int NL>
+__global__ void __launch_bounds__(256) fwt_small_kernel(const PassParams p) {
+  const bool im = blockIdx.y != 0;
+  const T* in = static_cast<const T*>(im ? p.in[1] : p.in[0]);
+  T* out = static_cast<T*>(im ? p.out[1] : p.out[0]);
+  const long long row = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= (p.comp_elems >> NL)) return;
+  T x[1 << NL];
+#pragma unroll
+  for (int i = 0; i < (1 << NL); ++i) x[i] = in[(row << NL) + i];
+  butterflies<(1u << NL) - 1u, A>(x);
+  if (p.do_scale) {
+#pragma unroll
+    for (int i = 0; i < (1 << NL); ++i) {
+      if constexpr (sizeof(T) == 4 && !std::is_integral<T>::value) x[i] = x[i] * p.scale_f32;
+      else if constexpr (sizeof(T) == 8) x[i] = x[i] * p.scale_f64;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < (1 << NL); ++i) out[(row << NL) + i] = x[i];
+}
+
+}  // namespace fwt

@@ -1,0 +1,22 @@
+// fp32 pass kernels (split complex fp32: each part is a real fp32 array).
+#include "../../include/fwt.h"
+#include "registry.cuh"
+
+namespace fwt {
+namespace {
+template <int... Ks> void rows(std::vector<KernelEntry>& v, std::integer_sequence<int, Ks...>) {
+  (v.push_back(row_entry<FWT_C32, 0, 2, Ks + 3>()), ...);
+}
+template <int... Ks> void cols(std::vector<KernelEntry>& v, std::integer_sequence<int, Ks...>) {
+  (v.push_back(col_entry<FWT_C32, 0, 2, Ks + 5>()), ...);
+}
+}  // namespace
+
+void register_c32(std::vector<KernelEntry>& v) {
+  v.push_back(small_entry<FWT_C32, float, ArithF32, 0>());
+  v.push_back(small_entry<FWT_C32, float, ArithF32, 1>());
+  v.push_back(small_entry<FWT_C32, float, ArithF32, 2>());
+  rows(v, std::make_integer_sequence<int, 13>{});  // K = 3 .. 15
+  cols(v, std::make_integer_sequence<int, 6>{});   // K = 5 .. 10
+}
+}  // namespace fwt

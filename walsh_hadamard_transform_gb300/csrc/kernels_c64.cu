@@ -1,0 +1,22 @@
+// fp64 pass kernels: exact int64 fixed-point butterflies (IEEE fp64 for tiles with Inf/NaN).
+#include "../../include/fwt.h"
+#include "registry.cuh"
+
+namespace fwt {
+namespace {
+template <int... Ks> void rows(std::vector<KernelEntry>& v, std::integer_sequence<int, Ks...>) {
+  (v.push_back(row_entry<FWT_C64, 1, 1, Ks + 3>()), ...);
+}
+template <int... Ks> void cols(std::vector<KernelEntry>& v, std::integer_sequence<int, Ks...>) {
+  (v.push_back(col_entry<FWT_C64, 1, 1, Ks + 6>()), ...);
+}
+}  // namespace
+
+void register_c64(std::vector<KernelEntry>& v) {
+  v.push_back(small_entry<FWT_C64, double, ArithF64, 0>());
+  v.push_back(small_entry<FWT_C64, double, ArithF64, 1>());
+  v.push_back(small_entry<FWT_C64, double, ArithF64, 2>());
+  rows(v, std::make_integer_sequence<int, 12>{});  // K = 3 .. 14
+  cols(v, std::make_integer_sequence<int, 5>{});   // K = 6 .. 10
+}
+}  // namespace fwt

@@ -1,0 +1,216 @@
+// Table of compiled pass kernels, their launchers and host-side shape checks.
+#pragma once
+
+#include <cstdint>
+#include <cstdio>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "fwt_kernels.cuh"
+
+namespace fwt {
+
+enum PassKind { KIND_SMALL = 0, KIND_ROW = 1, KIND_COL = 2 };
+
+struct KernelEntry {
+  int dtype;  // FWT_C32 / FWT_C64 / FWT_I32
+  int kind;   // PassKind
+  int K;      // transformed index bits of the pass
+  int TB;     // log2 elements per tile (0 for the small kernel)
+  int TS;     // first transformed tile bit (column tiles: log2 columns per tile)
+  int threads;
+  size_t smem;  // dynamic shared memory per CTA
+  cudaError_t (*launch)(const PassParams&, long long tiles, int ncomp, cudaStream_t);
+  cudaError_t (*setup)();  // per-device attributes; call with the device current
+  int (*selfcheck)();      // host-only index-map and bank-conflict check
+  const void* fn;
+};
+
+// Elements per thread for a tile of 2^TB elements: enough registers that the
+// three layouts exist (see tile_engine.cuh), at least 32.
+__host__ __device__ constexpr int choose_el(int TB, int LV) {
+  return (TB - 5 + LV + 1) / 2 > 5 ? (TB - 5 + LV + 1) / 2 : 5;
+}
+
+// ---- host-side checks of a tile shape ----------------------------------------------
+template <class S>
+uint32_t host_idx(int layout, uint32_t t, uint32_t r) {
+  return layout == 1 ? S::idx1(t, r) : layout == 2 ? S::idx2(t, r) : S::idx3(t, r);
+}
+
+// Shared-memory wavefronts of one warp-wide access: `bytes` per lane (4, 8 or 16).
+inline int smem_wavefronts(const uint32_t* byte_addr, int bytes) {
+  // lanes per phase: 32 for 4-byte, 16 for 8-byte, 8 for 16-byte accesses
+  const int per = bytes == 4 ? 32 : bytes == 8 ? 16 : 8;
+  int total = 0;
+  for (int ph = 0; ph < 32 / per; ++ph) {
+    int worst = 0;
+    for (int bank = 0; bank < 32; ++bank) {
+      std::vector<uint32_t> words;
+      for (int l = ph * per; l < (ph + 1) * per; ++l) {
+        for (int w = 0; w < bytes / 4; ++w) {
+          const uint32_t word = byte_addr[l] / 4 + w;
+          if ((int)(word % 32) != bank) continue;
+          bool dup = false;
+          for (uint32_t v : words) dup |= v == word;
+          if (!dup) words.push_back(word);
+        }
+      }
+      if ((int)words.size() > worst) worst = (int)words.size();
+    }
+    total += worst;
+  }
+  return total;
+}
+
+template <class S, bool COLS>
+int check_shape(const char* name) {
+  int fails = 0;
+  const uint32_t n = 1u << S::TB;
+  std::vector<uint8_t> seen(n);
+  // 1. each layout is a bijection (thread, register) -> tile index
+  for (int layout = 1; layout <= 3; ++layout) {
+    std::fill(seen.begin(), seen.end(), 0);
+    for (uint32_t t = 0; t < (uint32_t)S::NT; ++t)
+      for (uint32_t r = 0; r < (uint32_t)S::NE; ++r) {
+        const uint32_t u = host_idx<S>(layout, t, r);
+        if (u >= n || seen[u]++) {
+          if (fails < 4) fprintf(stderr, "fwt_selfcheck %s: layout %d not a bijection\n", name, layout);
+          ++fails;
+          t = S::NT; break;
+        }
+      }
+  }
+  // 2. register bit h of each layout flips tile bit rbit(layout, h)
+  for (int layout = 1; layout <= 3; ++layout)
+    for (int h = 0; h < S::EL; ++h)
+      for (uint32_t t = 0; t < (uint32_t)S::NT; t += 7)
+        for (uint32_t r = 0; r < (uint32_t)S::NE; ++r)
+          if (!((r >> h) & 1u) &&
+              host_idx<S>(layout, t, r | (1u << h)) != (host_idx<S>(layout, t, r) | (1u << S::rbit(layout, h)))) {
+            if (fails < 8) fprintf(stderr, "fwt_selfcheck %s: register bit map wrong\n", name);
+            ++fails;
+          }
+  // 3. the three rounds transform each bit of [TS, TS+TK) exactly once
+  if ((S::DONE1 & S::DONE2) || (S::DONE1 & S::DONE3) || (S::DONE2 & S::DONE3) ||
+      (S::DONE1 | S::DONE2 | S::DONE3) != S::TSET) {
+    fprintf(stderr, "fwt_selfcheck %s: rounds do not partition the transformed bits\n", name);
+    ++fails;
+  }
+  // 4. shared-memory accesses are conflict-free (one wavefront per phase)
+  const int esz = 16 / S::VEC;
+  uint32_t addr[32];
+  for (uint32_t w = 0; w < (uint32_t)S::NT / 32; ++w) {
+    for (int j = 0; j < S::NV; ++j) {  // L1 writes and L3 reads: 16-byte vectors
+      for (int layout = 1; layout <= 3; layout += 2) {
+        for (int l = 0; l < 32; ++l)
+          addr[l] = S::phys(host_idx<S>(layout, w * 32 + l, j * S::VEC)) * esz;
+        if (smem_wavefronts(addr, 16) != 4) {
+          if (fails < 12) fprintf(stderr, "fwt_selfcheck %s: bank conflict layout %d\n", name, layout);
+          ++fails;
+        }
+      }
+    }
+    for (int r = 0; r < S::NE; ++r) {  // L2 reads and writes: scalars
+      for (int l = 0; l < 32; ++l) addr[l] = S::phys(S::idx2(w * 32 + l, r)) * esz;
+      if (smem_wavefronts(addr, esz) != (esz == 4 ? 1 : 2)) {
+        if (fails < 12) fprintf(stderr, "fwt_selfcheck %s: bank conflict layout 2\n", name);
+        ++fails;
+      }
+    }
+  }
+  // 5. global accesses: every warp-wide 16-byte load (L1) and store (L3) fills
+  //    whole 32-byte sectors (row tiles: 512 contiguous bytes)
+  const int L = COLS ? S::TS + 3 : 0;  // any row stride >= the column width
+  for (int layout = 1; layout <= 3; layout += 2)
+    for (uint32_t w = 0; w < (uint32_t)S::NT / 32; ++w)
+      for (int j = 0; j < S::NV; ++j) {
+        std::vector<long long> sectors;
+        for (int l = 0; l < 32; ++l) {
+          const uint32_t u = host_idx<S>(layout, w * 32 + l, j * S::VEC);
+          long long off = COLS ? ((long long)(u >> S::TS) << L) + (u & ((1u << S::TS) - 1u)) : u;
+          const long long sec = off * esz / 32;
+          bool dup = false;
+          for (long long v : sectors) dup |= v == sec;
+          if (!dup) sectors.push_back(sec);
+        }
+        if ((int)sectors.size() != 16) {
+          if (fails < 16) fprintf(stderr, "fwt_selfcheck %s: uncoalesced global access\n", name);
+          ++fails;
+        }
+      }
+  return fails;
+}
+
+// ---- per-shape launch / setup ----------------------------------------------------------
+template <class S, int KIND, bool COLS>
+cudaError_t launch_tile(const PassParams& p, long long tiles, int ncomp, cudaStream_t st) {
+  const size_t smem = (size_t)(1u << S::TB) * (KIND == 1 || KIND == 3 ? 8 : 4);
+  fwt_tile_kernel<S, KIND, COLS><<<dim3((unsigned)tiles, (unsigned)ncomp), S::NT, smem, st>>>(p);
+  return cudaGetLastError();
+}
+template <class S, int KIND, bool COLS>
+cudaError_t setup_tile() {
+  const size_t smem = (size_t)(1u << S::TB) * (KIND == 1 || KIND == 3 ? 8 : 4);
+  return cudaFuncSetAttribute(fwt_tile_kernel<S, KIND, COLS>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+template <typename T, class A, int NL>
+cudaError_t launch_small(const PassParams& p, long long tiles, int ncomp, cudaStream_t st) {
+  fwt_small_kernel<T, A, NL><<<dim3((unsigned)tiles, (unsigned)ncomp), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+inline cudaError_t setup_none() { return cudaSuccess; }
+inline int selfcheck_none() { return 0; }
+
+// Row pass over bits [0, K): tiles of 2^max(K, 10) contiguous elements.
+template <int DT, int KIND, int LV, int K>
+KernelEntry row_entry() {
+  constexpr int TB = K > 10 ? K : 10;
+  constexpr int EL = choose_el(TB, LV);
+  using S = Shape<TB, 0, K, LV, TB - EL>;
+  KernelEntry e;
+  e.dtype = DT; e.kind = KIND_ROW; e.K = K; e.TB = TB; e.TS = 0; e.threads = S::NT;
+  e.smem = (size_t)(1u << TB) * (16 >> LV);
+  e.launch = &launch_tile<S, KIND, false>;
+  e.setup = &setup_tile<S, KIND, false>;
+  e.selfcheck = [] { return check_shape<S, false>("row"); };
+  e.fn = (const void*)&fwt_tile_kernel<S, KIND, false>;
+  return e;
+}
+
+// Column pass over bits [L, L + K): tiles of 2^K rows x 128 bytes of columns.
+template <int DT, int KIND, int LV, int K>
+KernelEntry col_entry() {
+  constexpr int CWL = LV + 3;  // 8 vectors of 16 bytes = 128 bytes of columns
+  constexpr int TB = K + CWL;
+  constexpr int EL = choose_el(TB, LV);
+  using S = Shape<TB, CWL, K, LV, TB - EL>;
+  KernelEntry e;
+  e.dtype = DT; e.kind = KIND_COL; e.K = K; e.TB = TB; e.TS = CWL; e.threads = S::NT;
+  e.smem = (size_t)(1u << TB) * (16 >> LV);
+  e.launch = &launch_tile<S, KIND, true>;
+  e.setup = &setup_tile<S, KIND, true>;
+  e.selfcheck = [] { return check_shape<S, true>("col"); };
+  e.fn = (const void*)&fwt_tile_kernel<S, KIND, true>;
+  return e;
+}
+
+template <int DT, typename T, class A, int NL>
+KernelEntry small_entry() {
+  KernelEntry e;
+  e.dtype = DT; e.kind = KIND_SMALL; e.K = NL; e.TB = 0; e.TS = 0; e.threads = 256; e.smem = 0;
+  e.launch = &launch_small<T, A, NL>;
+  e.setup = &setup_none;
+  e.selfcheck = &selfcheck_none;
+  e.fn = (const void*)&fwt_small_kernel<T, A, NL>;
+  return e;
+}
+
+void register_c32(std::vector<KernelEntry>& v);
+void register_c64(std::vector<KernelEntry>& v);
+void register_i32(std::vector<KernelEntry>& v);
+
+}  // namespace fwt

@@ -1,0 +1,173 @@
+// On-chip tile engine for the batched Walsh-Hadamard transform (sm_103a).
+//
+// A CTA owns one tile of 2^TB elements of one real array (the real or the
+// imaginary part of a batch of split complex vectors).  Within the tile the
+// transform acts on TK consecutive tile-index bits starting at bit TS; the other
+// tile-index bits are independent lanes of the same transform (several short
+// vectors packed into one tile, or the contiguous columns of a strided tile of
+// the Kronecker column pass).
+//
+// The butterfly network of the transform (iThome "Day 18" FWT post, section
+// "Tensor Core wants matrix multiplication": stage 0 local pairs, stage 1 stride
+// 2, stage 2 stride 4, ...) factors over index bits, and its stages commute, so
+// the stages may run in any order as long as every transformed bit gets exactly
+// one stage.  The tile moves through three register layouts:
+//
+//   L1  (load):  registers hold tile bits [0,LV) (one 16-byte vector) and the top
+//                E-LV bits; lanes hold bits [LV, LV+5); warps the rest.  Global
+//                loads are 16-byte vectors, 512 contiguous bytes per warp.
+//   L2:          registers hold bits [LV, LV+E); threads hold [0,LV) and the top.
+//   L3  (store): registers hold bits [0,LV) and [LV+5, E+5); lanes [LV, LV+5);
+//                warps the top.  Global stores are 16-byte vectors again.
+//
+// Each layout runs the butterflies of the register bits that are transformed and
+// not done yet; the two layout changes go through one XOR-swizzled shared-memory
+// buffer of the whole tile (iThome "Day 18" FWT post, intro: registers, warp
+// exchange and swizzled shared memory for the single-block path).  Each element
+// therefore costs one HBM read and one HBM write per pass.
+//
+// The swizzle XORs the low three bits of a 16-byte chunk index with the XOR-fold
+// of its higher 3-bit groups.  It keeps 16-byte vectors contiguous and makes the
+// vector accesses of L1/L3 and the scalar accesses of L2 free of bank conflicts
+// (checked on the host by fwt_selfcheck()).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fwt {
+
+__host__ __device__ constexpr int ilog2c(long long v) { return v <= 1 ? 0 : 1 + ilog2c(v >> 1); }
+
+// Swizzled 16-byte chunk index (GF(2)-linear, bijective on any power-of-two range).
+__host__ __device__ constexpr uint32_t swz_chunk(uint32_t c) {
+  return c ^ (((c >> 3) ^ (c >> 6) ^ (c >> 9) ^ (c >> 12) ^ (c >> 15)) & 7u);
+}
+
+// Compile-time description of one tile shape and its three layouts.
+//   TB: log2 elements per tile.  TS, TK: transformed tile bits [TS, TS+TK).
+//   LV: log2 elements per 16-byte vector.  PL: log2 threads per CTA.
+template <int TB_, int TS_, int TK_, int LV_, int PL_>
+struct Shape {
+  static constexpr int TB = TB_, TS = TS_, TK = TK_, LV = LV_, PL = PL_;
+  static constexpr int EL = TB - PL;  // log2 elements per thread
+  static constexpr int NT = 1 << PL, NE = 1 << EL, VEC = 1 << LV, NV = NE / VEC;
+  static_assert(PL >= 5, "at least one warp");
+  static_assert(EL >= 5, "L2 must hold the five lane bits of L1");
+  static_assert(LV <= PL && PL <= EL + 5 - LV, "L3 must hold the warp bits of L1");
+  static_assert(TS + TK <= TB, "transform bits inside the tile");
+
+  // element index (tile-local) of register r of thread t in each layout
+  __host__ __device__ static constexpr uint32_t idx1(uint32_t t, uint32_t r) {
+    return (r & (VEC - 1)) | (t << LV) | ((r >> LV) << (LV + PL));
+  }
+  __host__ __device__ static constexpr uint32_t idx2(uint32_t t, uint32_t r) {
+    return (t & (VEC - 1)) | (r << LV) | ((t >> LV) << (LV + EL));
+  }
+  __host__ __device__ static constexpr uint32_t idx3(uint32_t t, uint32_t r) {
+    return (r & (VEC - 1)) | ((t & 31u) << LV) | ((r >> LV) << (LV + 5)) | ((t >> 5) << (EL + 5));
+  }
+  // register bit h -> tile-index bit, per layout
+  __host__ __device__ static constexpr int rbit(int layout, int h) {
+    return layout == 1 ? (h < LV ? h : h + PL) : layout == 2 ? h + LV : (h < LV ? h : h + 5);
+  }
+  // tile-index bits held in registers by a layout
+  __host__ __device__ static constexpr uint32_t reg_elem_bits(int layout) {
+    uint32_t m = 0;
+    for (int h = 0; h < EL; ++h) m |= 1u << rbit(layout, h);
+    return m;
+  }
+  static constexpr uint32_t TSET = ((TK >= 32 ? 0u : (1u << TK)) - 1u) << TS;
+  static constexpr uint32_t DONE1 = reg_elem_bits(1) & TSET;
+  static constexpr uint32_t DONE2 = reg_elem_bits(2) & TSET & ~DONE1;
+  static constexpr uint32_t DONE3 = reg_elem_bits(3) & TSET & ~(DONE1 | DONE2);
+  static_assert((DONE1 | DONE2 | DONE3) == TSET, "every transformed bit gets one stage");
+  // the same sets as register-bit masks
+  __host__ __device__ static constexpr uint32_t reg_mask(int layout, uint32_t elem_set) {
+    uint32_t m = 0;
+    for (int h = 0; h < EL; ++h)
+      if ((elem_set >> rbit(layout, h)) & 1u) m |= 1u << h;
+    return m;
+  }
+  static constexpr uint32_t RM1 = reg_mask(1, DONE1);
+  static constexpr uint32_t RM2 = reg_mask(2, DONE2);
+  static constexpr uint32_t RM3 = reg_mask(3, DONE3);
+  // swizzled shared-memory element offset of a tile index
+  __host__ __device__ static constexpr uint32_t phys(uint32_t idx) {
+    return (swz_chunk(idx >> LV) << LV) | (idx & (VEC - 1));
+  }
+};
+
+// In-register butterflies over the register bits in MASK: pairs (r, r | 2^h) with
+// bit h of r clear become (a + b, a - b).
+template <uint32_t MASK, class A, int NE, typename U>
+__device__ __forceinline__ void butterflies(U (&x)[NE]) {
+#pragma unroll
+  for (int h = 0; h < ilog2c(NE); ++h) {
+    if ((MASK >> h) & 1u) {
+#pragma unroll
+      for (int r = 0; r < NE; ++r) {
+        if (!((r >> h) & 1)) {
+          const U a = x[r];
+          const U b = x[r | (1 << h)];
+          x[r] = A::add(a, b);
+          x[r | (1 << h)] = A::sub(a, b);
+        }
+      }
+    }
+  }
+}
+
+template <typename U> struct Vec16;
+template <> struct Vec16<float> { using type = float4; };
+template <> struct Vec16<uint32_t> { using type = uint4; };
+template <> struct Vec16<double> { using type = double2; };
+template <> struct Vec16<long long> { using type = longlong2; };
+
+// Store / load one 16-byte vector of registers x[j*VEC .. j*VEC+VEC-1].
+template <typename U, int VEC, int NE>
+__device__ __forceinline__ void put_vec(U* p, const U (&x)[NE], int j) {
+  using V = typename Vec16<U>::type;
+  V v;
+  U* pv = reinterpret_cast<U*>(&v);
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) pv[i] = x[j * VEC + i];
+  *reinterpret_cast<V*>(p) = v;
+}
+template <typename U, int VEC, int NE>
+__device__ __forceinline__ void get_vec(const U* p, U (&x)[NE], int j) {
+  using V = typename Vec16<U>::type;
+  const V v = *reinterpret_cast<const V*>(p);
+  const U* pv = reinterpret_cast<const U*>(&v);
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) x[j * VEC + i] = pv[i];
+}
+
+// Rounds 1-3 of the tile transform.  On entry x holds the tile in layout L1; on
+// exit it holds the transformed tile in layout L3.  `sm` is the tile-sized
+// shared buffer.  Starts with no pending shared-memory reads; ends with
+// __syncthreads() already passed for the buffer's last read.
+template <class S, class A, typename U>
+__device__ __forceinline__ void tile_rounds(U (&x)[S::NE], U* sm) {
+  const uint32_t t = threadIdx.x;
+  butterflies<S::RM1, A>(x);
+  // L1 -> shared (16-byte vectors)
+#pragma unroll
+  for (int j = 0; j < S::NV; ++j) put_vec<U, S::VEC>(sm + S::phys(S::idx1(t, j * S::VEC)), x, j);
+  __syncthreads();
+  // shared -> L2 (scalars)
+#pragma unroll
+  for (int r = 0; r < S::NE; ++r) x[r] = sm[S::phys(S::idx2(t, r))];
+  butterflies<S::RM2, A>(x);
+  __syncthreads();
+  // L2 -> shared (scalars)
+#pragma unroll
+  for (int r = 0; r < S::NE; ++r) sm[S::phys(S::idx2(t, r))] = x[r];
+  __syncthreads();
+  // shared -> L3 (16-byte vectors)
+#pragma unroll
+  for (int j = 0; j < S::NV; ++j) get_vec<U, S::VEC>(sm + S::phys(S::idx3(t, j * S::VEC)), x, j);
+  butterflies<S::RM3, A>(x);
+}
+
+}  // namespace fwt
