@@ -30,14 +30,18 @@ def gpu_transform(re, im, normalize, inplace=False):
 
 
 def rel_err_per_vector(gre, gim, ore, oim) -> np.ndarray:
-    """Complex relative L2 error of each vector (re and im together)."""
-    gre = gre.astype(np.float64); ore = ore.astype(np.float64)
-    num = np.sum((gre - ore) ** 2, axis=-1)
-    den = np.sum(ore ** 2, axis=-1)
+    """Complex relative L2 error of each vector (re and im together).
+
+    Both sides are divided by the vector's largest reference magnitude before
+    squaring, so entries near 1e300 neither overflow nor lose the ratio."""
+    gre = np.atleast_2d(gre).astype(np.float64); ore = np.atleast_2d(ore).astype(np.float64)
+    parts = [(gre, ore)]
     if gim is not None:
-        gim = gim.astype(np.float64); oim = oim.astype(np.float64)
-        num = num + np.sum((gim - oim) ** 2, axis=-1)
-        den = den + np.sum(oim ** 2, axis=-1)
+        parts.append((np.atleast_2d(gim).astype(np.float64), np.atleast_2d(oim).astype(np.float64)))
+    scale = np.max([np.max(np.abs(o), axis=-1) for _, o in parts], axis=0)
+    scale = np.where(scale > 0, scale, 1.0)[:, None]
+    num = sum(np.sum(((g - o) / scale) ** 2, axis=-1) for g, o in parts)
+    den = sum(np.sum((o / scale) ** 2, axis=-1) for _, o in parts)
     return np.sqrt(num) / np.where(den > 0, np.sqrt(den), 1.0)
 
 

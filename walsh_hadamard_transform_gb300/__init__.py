@@ -66,6 +66,10 @@ def library() -> ctypes.CDLL:
         lib.fwt_set_plan.restype = ci
         lib.fwt_selfcheck.argtypes = []
         lib.fwt_selfcheck.restype = ci
+        lib.fwt_set_column_bytes.argtypes = [ci, ci]
+        lib.fwt_set_column_bytes.restype = ci
+        lib.fwt_get_column_bytes.argtypes = [ci]
+        lib.fwt_get_column_bytes.restype = ci
         lib.fwt_trace_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ci]
         lib.fwt_trace_events.restype = ci
         lib.fwt_trace_count.argtypes = []
@@ -115,6 +119,17 @@ def set_plan(n: int, dtype: str, factors) -> None:
     st = library().fwt_set_plan(int(n), DTYPES[dtype], len(factors), buf)
     if st != FWT_OK:
         raise FwtError(st, f"fwt_set_plan(n={n}, {dtype}, {factors})")
+
+
+def set_column_bytes(dtype: str, nbytes: int) -> None:
+    """Column-pass segment width (64 or 128 bytes) for later plans of ``dtype``."""
+    st = library().fwt_set_column_bytes(DTYPES[dtype], int(nbytes))
+    if st != FWT_OK:
+        raise FwtError(st, f"fwt_set_column_bytes({dtype}, {nbytes})")
+
+
+def column_bytes(dtype: str) -> int:
+    return library().fwt_get_column_bytes(DTYPES[dtype])
 
 
 def selfcheck() -> int:

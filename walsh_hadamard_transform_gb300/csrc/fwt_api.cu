@@ -34,14 +34,14 @@ const std::vector<KernelEntry>& table() {
   return t;
 }
 
-const KernelEntry* find_kernel(int dtype, int kind, int K) {
+const KernelEntry* find_kernel(int dtype, int kind, int K, int col_bytes = 0) {
   for (const KernelEntry& e : table())
-    if (e.dtype == dtype && e.kind == kind && e.K == K) return &e;
+    if (e.dtype == dtype && e.kind == kind && e.K == K && (kind != KIND_COL || e.col_bytes == col_bytes))
+      return &e;
   return nullptr;
 }
 
 int elem_size(int dtype) { return dtype == FWT_C64 ? 8 : 4; }
-int col_width_log(int dtype) { return dtype == FWT_C64 ? 4 : 5; }  // 128-byte column segments
 
 // ---- plans -----------------------------------------------------------------------
 // A plan is the list of Kronecker factors H_n = H_{f_last} (x) ... (x) H_{f_0}, each
@@ -50,14 +50,17 @@ int col_width_log(int dtype) { return dtype == FWT_C64 ? 4 : 5; }  // 128-byte c
 struct Plan {
   int nf = 0;
   int bits[3] = {0, 0, 0};
+  int col_bytes = 128;  // width of the column passes' row segments
 };
 
 std::mutex g_plan_mu;
 Plan g_override[3][31];  // nf == 0: no override
+int g_col_bytes[3] = {64, 64, 64};  // default column segment width per dtype
 
 int max_row_bits(int dtype) { return dtype == FWT_C64 ? 14 : 15; }
-int min_col_bits(int dtype) { return dtype == FWT_C64 ? 6 : 5; }
-int max_col_bits(int) { return 10; }
+// column factors available for a segment width: tiles of 2^10 .. 2^15 (2^14 fp64) elements
+int min_col_bits(int dtype, int cb) { return (dtype == FWT_C64 ? 6 : 5) + (cb == 64 ? 1 : 0); }
+int max_col_bits(int, int cb) { return cb == 64 ? 11 : 10; }
 
 bool plan_valid(int n, int dtype, const Plan& p) {
   if (p.nf < 1 || p.nf > 3) return false;
@@ -71,8 +74,9 @@ bool plan_valid(int n, int dtype, const Plan& p) {
         return false;
       }
     } else {
-      if (!find_kernel(dtype, KIND_COL, k)) return false;
-      if (sum < col_width_log(dtype)) return false;  // a column segment must fit one row
+      const KernelEntry* e = find_kernel(dtype, KIND_COL, k, p.col_bytes);
+      if (!e) return false;
+      if (sum < e->TS) return false;  // a column segment must fit in one row
     }
     sum += k;
   }
@@ -81,7 +85,12 @@ bool plan_valid(int n, int dtype, const Plan& p) {
 
 Plan default_plan(int n, int dtype) {
   Plan p;
-  const int rmax = max_row_bits(dtype), cmin = min_col_bits(dtype), cmax = max_col_bits(dtype);
+  {
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    p.col_bytes = g_col_bytes[dtype];
+  }
+  const int rmax = max_row_bits(dtype), cmin = min_col_bits(dtype, p.col_bytes),
+            cmax = max_col_bits(dtype, p.col_bytes);
   if (n <= rmax) {
     p.nf = 1;
     p.bits[0] = n;
@@ -205,7 +214,7 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
       e = find_kernel(dtype, KIND_ROW, K);
       tiles = (comp_elems + (1ll << e->TB) - 1) >> e->TB;
     } else {
-      e = find_kernel(dtype, KIND_COL, K);
+      e = find_kernel(dtype, KIND_COL, K, plan.col_bytes);
       tiles = comp_elems >> e->TB;
     }
     if (tiles > INT_MAX) return FWT_ERR_UNSUPPORTED;
@@ -285,6 +294,10 @@ int fwt_set_plan(int n, int dtype, int nfactors, const int* bits) {
     return FWT_ERR_INVALID_ARG;
   fwt::Plan p;
   p.nf = nfactors;
+  {
+    std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
+    p.col_bytes = fwt::g_col_bytes[dtype];
+  }
   for (int f = 0; f < nfactors; ++f) {
     if (!bits) return FWT_ERR_INVALID_ARG;
     p.bits[f] = bits[f];
@@ -293,6 +306,19 @@ int fwt_set_plan(int n, int dtype, int nfactors, const int* bits) {
   std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
   fwt::g_override[dtype][n] = p;
   return FWT_OK;
+}
+
+int fwt_set_column_bytes(int dtype, int bytes) {
+  if (dtype < 0 || dtype > 2 || (bytes != 64 && bytes != 128)) return FWT_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
+  fwt::g_col_bytes[dtype] = bytes;
+  return FWT_OK;
+}
+
+int fwt_get_column_bytes(int dtype) {
+  if (dtype < 0 || dtype > 2) return -1;
+  std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
+  return fwt::g_col_bytes[dtype];
 }
 
 int fwt_trace_events(void** events, int capacity) {

@@ -178,32 +178,41 @@ __device__ __forceinline__ void plain_tile(const PassParams& p, unsigned char* s
 }
 
 // ---- fp64 in exact 64-bit fixed point -------------------------------------------
-// Biased exponent field used for scaling: subnormals and zeros count as 1.
-__device__ __forceinline__ uint32_t exp_key(long long bits) {
-  const uint32_t e = (uint32_t)((unsigned long long)bits >> 52) & 0x7ffu;
-  return e == 0x7ffu ? 0x800u : (e == 0 ? 1u : e);  // 0x800: Inf or NaN present
+// Tile-wide exponent scan: the largest high word without its sign bit carries the
+// largest biased exponent, and is >= 0x7ff00000 exactly when an Inf or NaN is
+// present.
+__device__ __forceinline__ uint32_t abs_hi(long long bits) {
+  return (uint32_t)((unsigned long long)bits >> 32) & 0x7fffffffu;
 }
 
-// q = round(v * 2^(F + 1023 - emax)) for |v| < 2^(emax - 1022): |q| <= 2^(F+1).
-__device__ __forceinline__ long long to_fixed(long long bits, int emax, int F) {
+// q = round(v * 2^(F + 1023 - emax)), ties away from zero, for |v| < 2^(emax - 1022):
+// |q| <= 2^(F+1).  Integer bit arithmetic only.
+template <int F>
+__device__ __forceinline__ long long to_fixed(long long bits, int emax) {
   const unsigned long long b = (unsigned long long)bits;
-  const int e = (int)((b >> 52) & 0x7ffu);
+  const int e = (int)((uint32_t)(b >> 32) >> 20) & 0x7ff;
   const unsigned long long m =
-      (b & 0x000fffffffffffffull) | (e ? 0x0010000000000000ull : 0ull);
-  const int sh = (e ? e : 1) - emax + F - 52;
+      (b & 0x000fffffffffffffull) | ((unsigned long long)(e != 0) << 52);
+  // v = m * 2^(max(e,1) - 1075), so q = m * 2^(max(e,1) - emax + F - 52)
+  const int sh = max(e, 1) - emax + F - 52;
   unsigned long long mag;
-  if (sh >= 0) {
+  if constexpr (F <= 52) {  // sh <= F - 52 <= 0: always a rounding right shift
+    const int rs = min(-sh, 63);
+    mag = (((m << 1) >> rs) + 1ull) >> 1;
+  } else if (sh >= 0) {
     mag = m << sh;
   } else {
-    const int rs1 = min(-sh - 1, 63);  // shift by (rs - 1), then round half up
-    mag = ((m >> rs1) + 1ull) >> 1;
+    const int rs = min(-sh, 63);
+    mag = (((m << 1) >> rs) + 1ull) >> 1;
   }
-  return (b >> 63) ? -(long long)mag : (long long)mag;
+  const unsigned long long neg = (unsigned long long)((long long)b >> 63);  // 0 or ~0
+  return (long long)((mag ^ neg) - neg);
 }
 
-// Rounds q * 2^e0 (optionally also / sqrt 2) to the nearest fp64, ties to even.
-__device__ __forceinline__ long long from_fixed(long long q, int e0, int half,
-                                                unsigned long long rsqrt2) {
+// Exact rounding of q * 2^e0 (optionally also / sqrt 2) to the nearest fp64, ties
+// to even, including subnormal results and overflow to Inf.
+__device__ __forceinline__ long long from_fixed_exact(long long q, int e0, int half,
+                                                      unsigned long long rsqrt2) {
   const unsigned long long sign = (unsigned long long)q & 0x8000000000000000ull;
   unsigned long long a = q < 0 ? (unsigned long long)(-q) : (unsigned long long)q;
   if (half) a = __umul64hi(a, rsqrt2);  // a / sqrt(2), truncated (error < 1 unit)
@@ -239,6 +248,22 @@ __device__ __forceinline__ long long from_fixed(long long q, int e0, int half,
   return (long long)(sign | t);
 }
 
+// The same rounding through the hardware int64 -> fp64 conversion (round to
+// nearest even; it runs on the fp64 unit, beside the integer pipes), followed by an
+// exact power-of-two rescale done as an add to the exponent field.  Valid when
+// every nonzero result is a normal number: -1022 <= e0 <= 960 (|q| < 2^63).
+// e0_field = e0 << 52.  `half` (uniform) also divides by sqrt(2) first.
+__device__ __forceinline__ long long from_fixed_cvt(long long q, long long e0_field, int half,
+                                                    unsigned long long rsqrt2) {
+  if (half) {
+    const unsigned long long neg = (unsigned long long)(q >> 63);
+    const unsigned long long a = __umul64hi(((unsigned long long)q ^ neg) - neg, rsqrt2);
+    q = (long long)((a ^ neg) - neg);
+  }
+  const long long b = __double_as_longlong(__ll2double_rn(q));
+  return q == 0 ? 0ll : b + e0_field;
+}
+
 template <class S, bool COLS>
 __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* smem_raw) {
   __shared__ uint32_t red[32];
@@ -249,16 +274,16 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
   long long x[S::NE];
   load_tile<S, COLS>(reinterpret_cast<const long long*>(in), m, x);
   // tile-wide largest exponent (and whether any Inf/NaN is present)
-  uint32_t key = 1;
+  uint32_t key = 0;
 #pragma unroll
-  for (int r = 0; r < S::NE; ++r) key = max(key, exp_key(x[r]));
+  for (int r = 0; r < S::NE; ++r) key = max(key, abs_hi(x[r]));
   key = __reduce_max_sync(0xffffffffu, key);
   if ((threadIdx.x & 31u) == 0) red[threadIdx.x >> 5] = key;
   __syncthreads();
   key = red[0];
 #pragma unroll
   for (int w = 1; w < S::NT / 32; ++w) key = max(key, red[w]);
-  if (key >= 0x800u) {  // IEEE path for tiles with Inf/NaN
+  if (key >= 0x7ff00000u) {  // IEEE path for tiles with Inf/NaN
     double xd[S::NE];
 #pragma unroll
     for (int r = 0; r < S::NE; ++r) xd[r] = __longlong_as_double(x[r]);
@@ -270,15 +295,23 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
     store_tile<S, COLS>(out, m, xd);
     return;
   }
-  const int emax = (int)key;
+  const int emax = max((int)(key >> 20), 1);  // zeros and subnormals scale as exponent 1
   constexpr int F = 61 - S::TK;  // headroom: |q| <= 2^(F+1) grows by 2^TK
 #pragma unroll
-  for (int r = 0; r < S::NE; ++r) x[r] = to_fixed(x[r], emax, F);
+  for (int r = 0; r < S::NE; ++r) x[r] = to_fixed<F>(x[r], emax);
   tile_rounds<S, ArithI64>(x, reinterpret_cast<long long*>(smem_raw));
   const int e0 = emax - 1023 - F + (p.do_scale ? p.scale_exp : 0);
   const int half = p.do_scale ? p.scale_half : 0;
+  // every nonzero |q| lies in [1, 2^63): results are normal numbers iff
+  // 1 <= e0 + 1023 and e0 + 1023 + 63 <= 2046 (uniform over the tile)
+  if (e0 >= -1022 && e0 <= 960) {
+    const long long e0_field = (long long)((unsigned long long)(long long)e0 << 52);
 #pragma unroll
-  for (int r = 0; r < S::NE; ++r) x[r] = from_fixed(x[r], e0, half, p.rsqrt2_q64);
+    for (int r = 0; r < S::NE; ++r) x[r] = from_fixed_cvt(x[r], e0_field, half, p.rsqrt2_q64);
+  } else {
+#pragma unroll
+    for (int r = 0; r < S::NE; ++r) x[r] = from_fixed_exact(x[r], e0, half, p.rsqrt2_q64);
+  }
   store_tile<S, COLS>(reinterpret_cast<long long*>(out), m, x);
 }
 

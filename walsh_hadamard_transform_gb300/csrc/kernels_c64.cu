@@ -7,8 +7,8 @@ namespace {
 template <int... Ks> void rows(std::vector<KernelEntry>& v, std::integer_sequence<int, Ks...>) {
   (v.push_back(row_entry<FWT_C64, 1, 1, Ks + 3>()), ...);
 }
-template <int... Ks> void cols(std::vector<KernelEntry>& v, std::integer_sequence<int, Ks...>) {
-  (v.push_back(col_entry<FWT_C64, 1, 1, Ks + 6>()), ...);
+template <int CB, int K0, int... Ks> void cols(std::vector<KernelEntry>& v, std::integer_sequence<int, Ks...>) {
+  (v.push_back(col_entry<FWT_C64, 1, 1, Ks + K0, CB>()), ...);
 }
 }  // namespace
 
@@ -17,6 +17,7 @@ void register_c64(std::vector<KernelEntry>& v) {
   v.push_back(small_entry<FWT_C64, double, ArithF64, 1>());
   v.push_back(small_entry<FWT_C64, double, ArithF64, 2>());
   rows(v, std::make_integer_sequence<int, 12>{});  // K = 3 .. 14
-  cols(v, std::make_integer_sequence<int, 5>{});   // K = 6 .. 10
+  cols<128, 6>(v, std::make_integer_sequence<int, 5>{});  // K = 6 .. 10
+  cols<64, 7>(v, std::make_integer_sequence<int, 5>{});   // K = 7 .. 11
 }
 }  // namespace fwt

@@ -7,8 +7,8 @@ namespace {
 template <int... Ks> void rows(std::vector<KernelEntry>& v, std::integer_sequence<int, Ks...>) {
   (v.push_back(row_entry<FWT_I32, 2, 2, Ks + 3>()), ...);
 }
-template <int... Ks> void cols(std::vector<KernelEntry>& v, std::integer_sequence<int, Ks...>) {
-  (v.push_back(col_entry<FWT_I32, 2, 2, Ks + 5>()), ...);
+template <int CB, int K0, int... Ks> void cols(std::vector<KernelEntry>& v, std::integer_sequence<int, Ks...>) {
+  (v.push_back(col_entry<FWT_I32, 2, 2, Ks + K0, CB>()), ...);
 }
 }  // namespace
 
@@ -17,6 +17,7 @@ void register_i32(std::vector<KernelEntry>& v) {
   v.push_back(small_entry<FWT_I32, uint32_t, ArithU32, 1>());
   v.push_back(small_entry<FWT_I32, uint32_t, ArithU32, 2>());
   rows(v, std::make_integer_sequence<int, 13>{});  // K = 3 .. 15
-  cols(v, std::make_integer_sequence<int, 6>{});   // K = 5 .. 10
+  cols<128, 5>(v, std::make_integer_sequence<int, 6>{});  // K = 5 .. 10
+  cols<64, 6>(v, std::make_integer_sequence<int, 6>{});   // K = 6 .. 11
 }
 }  // namespace fwt

@@ -19,6 +19,7 @@ struct KernelEntry {
   int K;      // transformed index bits of the pass
   int TB;     // log2 elements per tile (0 for the small kernel)
   int TS;     // first transformed tile bit (column tiles: log2 columns per tile)
+  int col_bytes;  // column tiles: bytes of contiguous columns per row (64 or 128)
   int threads;
   size_t smem;  // dynamic shared memory per CTA
   cudaError_t (*launch)(const PassParams&, long long tiles, int ncomp, cudaStream_t);
@@ -172,7 +173,8 @@ KernelEntry row_entry() {
   constexpr int EL = choose_el(TB, LV);
   using S = Shape<TB, 0, K, LV, TB - EL>;
   KernelEntry e;
-  e.dtype = DT; e.kind = KIND_ROW; e.K = K; e.TB = TB; e.TS = 0; e.threads = S::NT;
+  e.dtype = DT; e.kind = KIND_ROW; e.K = K; e.TB = TB; e.TS = 0; e.col_bytes = 0;
+  e.threads = S::NT;
   e.smem = (size_t)(1u << TB) * (16 >> LV);
   e.launch = &launch_tile<S, KIND, false>;
   e.setup = &setup_tile<S, KIND, false>;
@@ -181,15 +183,17 @@ KernelEntry row_entry() {
   return e;
 }
 
-// Column pass over bits [L, L + K): tiles of 2^K rows x 128 bytes of columns.
-template <int DT, int KIND, int LV, int K>
+// Column pass over bits [L, L + K): tiles of 2^K rows x CB bytes of columns
+// (CB = 64 or 128: four or eight 16-byte vectors).
+template <int DT, int KIND, int LV, int K, int CB>
 KernelEntry col_entry() {
-  constexpr int CWL = LV + 3;  // 8 vectors of 16 bytes = 128 bytes of columns
+  constexpr int CWL = LV + (CB == 128 ? 3 : 2);
   constexpr int TB = K + CWL;
   constexpr int EL = choose_el(TB, LV);
   using S = Shape<TB, CWL, K, LV, TB - EL>;
   KernelEntry e;
-  e.dtype = DT; e.kind = KIND_COL; e.K = K; e.TB = TB; e.TS = CWL; e.threads = S::NT;
+  e.dtype = DT; e.kind = KIND_COL; e.K = K; e.TB = TB; e.TS = CWL; e.col_bytes = CB;
+  e.threads = S::NT;
   e.smem = (size_t)(1u << TB) * (16 >> LV);
   e.launch = &launch_tile<S, KIND, true>;
   e.setup = &setup_tile<S, KIND, true>;
@@ -201,7 +205,8 @@ KernelEntry col_entry() {
 template <int DT, typename T, class A, int NL>
 KernelEntry small_entry() {
   KernelEntry e;
-  e.dtype = DT; e.kind = KIND_SMALL; e.K = NL; e.TB = 0; e.TS = 0; e.threads = 256; e.smem = 0;
+  e.dtype = DT; e.kind = KIND_SMALL; e.K = NL; e.TB = 0; e.TS = 0; e.col_bytes = 0;
+  e.threads = 256; e.smem = 0;
   e.launch = &launch_small<T, A, NL>;
   e.setup = &setup_none;
   e.selfcheck = &selfcheck_none;
