@@ -96,17 +96,28 @@ def test_plans(lib):
 
 def test_plan_override_roundtrip(lib):
     default = fwt.plan_factors(20, "c32")
-    fwt.set_plan(20, "c32", [10, 5, 5])
+    width = fwt.column_bytes("c32")
+    fwt.set_column_bytes("c32", 128)  # 5-bit column factors exist for 128-byte tiles
     try:
+        fwt.set_plan(20, "c32", [10, 5, 5])
         assert fwt.plan_factors(20, "c32") == [10, 5, 5]
         assert fwt.plan_passes(20, "c32") == 3
     finally:
         fwt.set_plan(20, "c32", None)
+        fwt.set_column_bytes("c32", width)
     assert fwt.plan_factors(20, "c32") == default
-    for bad in ([10, 9], [16, 4], [2, 18], [4, 6, 10], [10, 11]):
+    for bad in ([10, 9], [16, 4], [2, 18], [4, 6, 10], [10, 11], [10, 5, 5]):
         with pytest.raises(fwt.FwtError):
             fwt.set_plan(20, "c32", bad)
     assert fwt.plan_factors(20, "c32") == default
+
+
+def test_column_bytes_setting(lib):
+    for dt in ("c32", "c64", "i32"):
+        assert fwt.column_bytes(dt) in (64, 128)
+    with pytest.raises(fwt.FwtError):
+        fwt.set_column_bytes("c32", 96)
+    assert lib.fwt_get_column_bytes(5) == -1
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
