@@ -106,7 +106,7 @@ def test_plan_override_roundtrip(lib):
         fwt.set_plan(20, "c32", None)
         fwt.set_column_bytes("c32", width)
     assert fwt.plan_factors(20, "c32") == default
-    for bad in ([10, 9], [16, 4], [2, 18], [4, 6, 10], [10, 11], [10, 5, 5]):
+    for bad in ([10, 9], [16, 4], [2, 18], [3, 7, 10], [10, 11], [10, 5, 5]):
         with pytest.raises(fwt.FwtError):
             fwt.set_plan(20, "c32", bad)
     assert fwt.plan_factors(20, "c32") == default
