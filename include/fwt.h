@@ -120,12 +120,12 @@ int fwt_plan_factors(int n, int dtype, int* bits, int max_factors);
 int fwt_set_plan(int n, int dtype, int nfactors, const int* bits);
 
 /*
- * Tuning: bytes of contiguous columns (64 or 128) that each tile of a column
- * pass reads from every row it touches.  Wider segments make longer DRAM
- * bursts; narrower ones halve the tile and let two CTAs share an SM.  Affects
- * default plans and plans set afterwards for `dtype`.  Returns FWT_OK or
- * FWT_ERR_INVALID_ARG; fwt_get_column_bytes returns the current width (-1 for
- * an invalid dtype).
+ * Tuning: bytes of contiguous columns (64 or 128; also 32 for FWT_C64) that each
+ * tile of a column pass reads from every row it touches.  Wider segments make
+ * longer DRAM bursts; narrower ones shrink the tile so that two CTAs share an SM.
+ * Affects default plans and plans set afterwards for `dtype`.  Returns FWT_OK or
+ * FWT_ERR_INVALID_ARG; fwt_get_column_bytes returns the current width (-1 for an
+ * invalid dtype).
  */
 int fwt_set_column_bytes(int dtype, int bytes);
 int fwt_get_column_bytes(int dtype);

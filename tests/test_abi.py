@@ -90,7 +90,7 @@ def test_plans(lib):
             assert fwt.plan_passes(n, dt) == len(f)
             assert (len(f) == 1) == (n <= rmax)
     assert fwt.plan_factors(24, "c32") == [14, 10]
-    assert fwt.plan_factors(24, "c64") == [14, 10]
+    assert fwt.plan_factors(24, "c64") == [13, 11]
     assert lib.fwt_plan_passes(31, 0) == -1 and lib.fwt_plan_passes(10, 7) == -1
 
 
@@ -114,9 +114,11 @@ def test_plan_override_roundtrip(lib):
 
 def test_column_bytes_setting(lib):
     for dt in ("c32", "c64", "i32"):
-        assert fwt.column_bytes(dt) in (64, 128)
+        assert fwt.column_bytes(dt) in (32, 64, 128)
     with pytest.raises(fwt.FwtError):
         fwt.set_column_bytes("c32", 96)
+    with pytest.raises(fwt.FwtError):
+        fwt.set_column_bytes("c32", 32)  # 32-byte column tiles exist for fp64 only
     assert lib.fwt_get_column_bytes(5) == -1
 
 

@@ -55,12 +55,14 @@ struct Plan {
 
 std::mutex g_plan_mu;
 Plan g_override[3][31];  // nf == 0: no override
-int g_col_bytes[3] = {64, 64, 64};  // default column segment width per dtype
+int g_col_bytes[3] = {64, 32, 64};  // default column segment width per dtype
 
 int max_row_bits(int dtype) { return dtype == FWT_C64 ? 14 : 15; }
 // column factors available for a segment width: tiles of 2^10 .. 2^15 (2^14 fp64) elements
-int min_col_bits(int dtype, int cb) { return (dtype == FWT_C64 ? 6 : 5) + (cb == 64 ? 1 : 0); }
-int max_col_bits(int, int cb) { return cb == 64 ? 11 : 10; }
+int min_col_bits(int dtype, int cb) {
+  return (dtype == FWT_C64 ? 6 : 5) + (cb == 64 ? 1 : cb == 32 ? 2 : 0);
+}
+int max_col_bits(int, int cb) { return cb == 128 ? 10 : cb == 64 ? 11 : 12; }
 
 bool plan_valid(int n, int dtype, const Plan& p) {
   if (p.nf < 1 || p.nf > 3) return false;
@@ -96,7 +98,8 @@ Plan default_plan(int n, int dtype) {
     p.bits[0] = n;
     return p;
   }
-  const int row_pref = 14;  // 64 KiB (fp32) / 128 KiB (fp64) row tiles
+  // preferred row factor: 64 KiB row tiles for large n; smaller n splits near 12 + rest
+  const int row_pref = n >= 22 ? (dtype == FWT_C64 ? 13 : 14) : 12;
   if (n <= rmax + cmax) {
     int a = std::min(std::max(cmin, n - row_pref), cmax);
     if (n - a > rmax) a = n - rmax;
@@ -309,7 +312,9 @@ int fwt_set_plan(int n, int dtype, int nfactors, const int* bits) {
 }
 
 int fwt_set_column_bytes(int dtype, int bytes) {
-  if (dtype < 0 || dtype > 2 || (bytes != 64 && bytes != 128)) return FWT_ERR_INVALID_ARG;
+  if (dtype < 0 || dtype > 2 || (bytes != 32 && bytes != 64 && bytes != 128) ||
+      (bytes == 32 && dtype != FWT_C64))
+    return FWT_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
   fwt::g_col_bytes[dtype] = bytes;
   return FWT_OK;

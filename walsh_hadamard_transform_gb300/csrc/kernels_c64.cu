@@ -19,5 +19,6 @@ void register_c64(std::vector<KernelEntry>& v) {
   rows(v, std::make_integer_sequence<int, 12>{});  // K = 3 .. 14
   cols<128, 6>(v, std::make_integer_sequence<int, 5>{});  // K = 6 .. 10
   cols<64, 7>(v, std::make_integer_sequence<int, 5>{});   // K = 7 .. 11
+  cols<32, 8>(v, std::make_integer_sequence<int, 5>{});   // K = 8 .. 12
 }
 }  // namespace fwt

@@ -99,7 +99,23 @@ int check_shape(const char* name) {
     fprintf(stderr, "fwt_selfcheck %s: rounds do not partition the transformed bits\n", name);
     ++fails;
   }
-  // 4. shared-memory accesses are conflict-free (one wavefront per phase)
+  // 4a. the kernels' table-based shared-memory offsets equal the swizzle map
+  for (uint32_t t = 0; t < (uint32_t)S::NT; ++t) {
+    uint32_t tab[8];
+    bool ok = true;
+    S::table1(t, tab);
+    for (int j = 0; j < S::NV; ++j) ok &= tab[S::h1(j)] + S::c1(j) == S::phys(S::idx1(t, j * S::VEC));
+    S::table2(t, tab);
+    for (int r = 0; r < S::NE; ++r) ok &= tab[S::h2(r)] + S::c2(r) == S::phys(S::idx2(t, r));
+    S::table3(t, tab);
+    for (int j = 0; j < S::NV; ++j) ok &= tab[S::h3(j)] + S::c3(j) == S::phys(S::idx3(t, j * S::VEC));
+    if (!ok) {
+      if (fails < 12) fprintf(stderr, "fwt_selfcheck %s: shared-memory address table wrong\n", name);
+      ++fails;
+      break;
+    }
+  }
+  // 4b. shared-memory accesses are conflict-free (one wavefront per phase)
   const int esz = 16 / S::VEC;
   uint32_t addr[32];
   for (uint32_t w = 0; w < (uint32_t)S::NT / 32; ++w) {
@@ -184,10 +200,10 @@ KernelEntry row_entry() {
 }
 
 // Column pass over bits [L, L + K): tiles of 2^K rows x CB bytes of columns
-// (CB = 64 or 128: four or eight 16-byte vectors).
+// (CB = 32, 64 or 128: two, four or eight 16-byte vectors).
 template <int DT, int KIND, int LV, int K, int CB>
 KernelEntry col_entry() {
-  constexpr int CWL = LV + (CB == 128 ? 3 : 2);
+  constexpr int CWL = LV + (CB == 128 ? 3 : CB == 64 ? 2 : 1);
   constexpr int TB = K + CWL;
   constexpr int EL = choose_el(TB, LV);
   using S = Shape<TB, CWL, K, LV, TB - EL>;

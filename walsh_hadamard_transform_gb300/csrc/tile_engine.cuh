@@ -96,6 +96,41 @@ struct Shape {
   __host__ __device__ static constexpr uint32_t phys(uint32_t idx) {
     return (swz_chunk(idx >> LV) << LV) | (idx & (VEC - 1));
   }
+
+  // The same offsets, split into a per-thread table of 8 values and a
+  // compile-time constant per register, so each shared-memory access needs no
+  // address arithmetic.  The swizzle is linear over XOR and the thread and
+  // register parts of a chunk index occupy disjoint bits, so
+  //   phys = table[h(register)] + const(register),
+  // where the table entry absorbs the thread's part of the 3-bit XOR.
+  __host__ __device__ static constexpr uint32_t fold7(uint32_t v) {
+    return (v ^ (v >> 3) ^ (v >> 6) ^ (v >> 9) ^ (v >> 12)) & 7u;
+  }
+  // layout 1, vector j: chunk = t | j << PL
+  __host__ __device__ static void table1(uint32_t t, uint32_t (&tab)[8]) {
+    const uint32_t lo = (t & 7u) ^ fold7(t >> 3);
+    for (uint32_t h = 0; h < 8; ++h) tab[h] = ((t & ~7u) + (lo ^ h)) << LV;
+  }
+  __host__ __device__ static constexpr uint32_t h1(int j) { return fold7((uint32_t)j << (PL - 3)); }
+  __host__ __device__ static constexpr uint32_t c1(int j) { return ((uint32_t)j << PL) << LV; }
+  // layout 2, register r: chunk = r | (t >> LV) << EL, plus the element within the vector
+  __host__ __device__ static void table2(uint32_t t, uint32_t (&tab)[8]) {
+    const uint32_t tt = (t >> LV) << EL;
+    const uint32_t g = fold7(tt >> 3);
+    for (uint32_t h = 0; h < 8; ++h) tab[h] = ((tt + (h ^ g)) << LV) + (t & (VEC - 1));
+  }
+  __host__ __device__ static constexpr uint32_t h2(int r) {
+    return ((uint32_t)r & 7u) ^ fold7((uint32_t)r >> 3);
+  }
+  __host__ __device__ static constexpr uint32_t c2(int r) { return ((uint32_t)r & ~7u) << LV; }
+  // layout 3, vector j: chunk = (t & 31) | j << 5 | (t >> 5) << (EL + 5 - LV)
+  __host__ __device__ static void table3(uint32_t t, uint32_t (&tab)[8]) {
+    const uint32_t lp = t & 31u, wp = (t >> 5) << (EL + 5 - LV);
+    const uint32_t g = fold7(lp >> 3) ^ fold7(wp >> 3);
+    for (uint32_t h = 0; h < 8; ++h) tab[h] = (wp + (lp & ~7u) + ((lp & 7u) ^ g ^ h)) << LV;
+  }
+  __host__ __device__ static constexpr uint32_t h3(int j) { return fold7((uint32_t)j << 2); }
+  __host__ __device__ static constexpr uint32_t c3(int j) { return ((uint32_t)j << 5) << LV; }
 };
 
 // In-register butterflies over the register bits in MASK: pairs (r, r | 2^h) with
@@ -145,28 +180,32 @@ __device__ __forceinline__ void get_vec(const U* p, U (&x)[NE], int j) {
 
 // Rounds 1-3 of the tile transform.  On entry x holds the tile in layout L1; on
 // exit it holds the transformed tile in layout L3.  `sm` is the tile-sized
-// shared buffer.  Starts with no pending shared-memory reads; ends with
-// __syncthreads() already passed for the buffer's last read.
+// shared buffer; nothing may be pending on it on entry, and its last reads (the
+// L3 loads) are not yet fenced by a barrier on exit.
 template <class S, class A, typename U>
 __device__ __forceinline__ void tile_rounds(U (&x)[S::NE], U* sm) {
   const uint32_t t = threadIdx.x;
+  uint32_t tab[8];
   butterflies<S::RM1, A>(x);
   // L1 -> shared (16-byte vectors)
+  S::table1(t, tab);
 #pragma unroll
-  for (int j = 0; j < S::NV; ++j) put_vec<U, S::VEC>(sm + S::phys(S::idx1(t, j * S::VEC)), x, j);
+  for (int j = 0; j < S::NV; ++j) put_vec<U, S::VEC>(sm + tab[S::h1(j)] + S::c1(j), x, j);
   __syncthreads();
   // shared -> L2 (scalars)
+  S::table2(t, tab);
 #pragma unroll
-  for (int r = 0; r < S::NE; ++r) x[r] = sm[S::phys(S::idx2(t, r))];
+  for (int r = 0; r < S::NE; ++r) x[r] = sm[tab[S::h2(r)] + S::c2(r)];
   butterflies<S::RM2, A>(x);
   __syncthreads();
   // L2 -> shared (scalars)
 #pragma unroll
-  for (int r = 0; r < S::NE; ++r) sm[S::phys(S::idx2(t, r))] = x[r];
+  for (int r = 0; r < S::NE; ++r) sm[tab[S::h2(r)] + S::c2(r)] = x[r];
   __syncthreads();
   // shared -> L3 (16-byte vectors)
+  S::table3(t, tab);
 #pragma unroll
-  for (int j = 0; j < S::NV; ++j) get_vec<U, S::VEC>(sm + S::phys(S::idx3(t, j * S::VEC)), x, j);
+  for (int j = 0; j < S::NV; ++j) get_vec<U, S::VEC>(sm + tab[S::h3(j)] + S::c3(j), x, j);
   butterflies<S::RM3, A>(x);
 }
 
