@@ -131,6 +131,19 @@ int fwt_set_column_bytes(int dtype, int bytes);
 int fwt_get_column_bytes(int dtype);
 
 /*
+ * L2 chunking of multi-pass transforms (tuning): when a plan has two or more
+ * passes, the library runs all passes on one group of whole vectors before the
+ * next group, so each intermediate is read back from L2 rather than DRAM.  A
+ * group holds as many vectors as fit `bytes` (both parts in one launch when a
+ * re/im pair fits, else one part at a time).  bytes = -1: half the L2 of the
+ * current device; 0 (default): no chunking (one launch per pass over the batch).
+ * Vectors larger than the budget are never chunked.  Process-wide; returns
+ * FWT_OK or FWT_ERR_INVALID_ARG.  fwt_get_l2_chunk_bytes returns the setting.
+ */
+int fwt_set_l2_chunk_bytes(long long bytes);
+long long fwt_get_l2_chunk_bytes(void);
+
+/*
  * Per-pass tracing with caller-owned CUDA events (tracing without a profiler).
  * fwt_trace_events(events, capacity) arms tracing for the calling host thread:
  * every pass launched afterwards by this thread is bracketed by two

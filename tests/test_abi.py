@@ -127,3 +127,12 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(fwt, "LIBRARY", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         fwt.library()
+
+
+def test_l2_chunk_setting(lib):
+    assert fwt.l2_chunk_bytes() == 0
+    fwt.set_l2_chunk_bytes(-1)
+    assert fwt.l2_chunk_bytes() == -1
+    fwt.set_l2_chunk_bytes(0)
+    with pytest.raises(fwt.FwtError):
+        fwt.set_l2_chunk_bytes(-2)

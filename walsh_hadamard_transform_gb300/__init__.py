@@ -70,6 +70,10 @@ def library() -> ctypes.CDLL:
         lib.fwt_set_column_bytes.restype = ci
         lib.fwt_get_column_bytes.argtypes = [ci]
         lib.fwt_get_column_bytes.restype = ci
+        lib.fwt_set_l2_chunk_bytes.argtypes = [ctypes.c_longlong]
+        lib.fwt_set_l2_chunk_bytes.restype = ci
+        lib.fwt_get_l2_chunk_bytes.argtypes = []
+        lib.fwt_get_l2_chunk_bytes.restype = ctypes.c_longlong
         lib.fwt_trace_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ci]
         lib.fwt_trace_events.restype = ci
         lib.fwt_trace_count.argtypes = []
@@ -130,6 +134,17 @@ def set_column_bytes(dtype: str, nbytes: int) -> None:
 
 def column_bytes(dtype: str) -> int:
     return library().fwt_get_column_bytes(DTYPES[dtype])
+
+
+def set_l2_chunk_bytes(nbytes: int) -> None:
+    """L2 chunk budget for multi-pass transforms: -1 = half the L2, 0 = off (default)."""
+    st = library().fwt_set_l2_chunk_bytes(int(nbytes))
+    if st != FWT_OK:
+        raise FwtError(st, f"fwt_set_l2_chunk_bytes({nbytes})")
+
+
+def l2_chunk_bytes() -> int:
+    return library().fwt_get_l2_chunk_bytes()
 
 
 def selfcheck() -> int:

@@ -130,6 +130,16 @@ Plan get_plan(int n, int dtype) {
 // ---- per-device set-up -------------------------------------------------------------
 std::mutex g_dev_mu;
 std::vector<char> g_dev_ready;
+std::vector<long long> g_dev_l2;  // L2 bytes per device
+long long g_chunk_bytes = 0;       // -1: half the L2 of the current device; 0: off (default)
+
+long long chunk_budget() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (g_chunk_bytes >= 0) return g_chunk_bytes;
+  return dev < (int)g_dev_l2.size() ? g_dev_l2[dev] / 2 : 0;
+}
 
 cudaError_t ensure_device() {
   int dev = 0;
@@ -142,6 +152,11 @@ cudaError_t ensure_device() {
     err = e.setup();
     if (err != cudaSuccess) return err;
   }
+  int l2 = 0;
+  err = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+  if (err != cudaSuccess) return err;
+  if ((int)g_dev_l2.size() <= dev) g_dev_l2.resize(dev + 1, 0);
+  g_dev_l2[dev] = l2;
   g_dev_ready[dev] = 1;
   return cudaSuccess;
 }
@@ -197,54 +212,90 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
   }
 
   PassParams p{};
-  p.comp_elems = comp_elems;
   const double s = n % 2 == 0 ? std::ldexp(1.0, -n / 2) : std::ldexp(1.0, -(n - 1) / 2) / std::sqrt(2.0);
   p.scale_f64 = s;
   p.scale_f32 = (float)s;
   p.scale_exp = -(n / 2);
   p.scale_half = n % 2;
   p.rsqrt2_q64 = rsqrt2_q64();
-  const int ncomp = has_im ? 2 : 1;
-  int L = 0;
-  for (int f = 0; f < plan.nf; ++f) {
-    const int K = plan.bits[f];
-    const KernelEntry* e;
-    long long tiles;
-    if (f == 0 && K <= 2) {
-      e = find_kernel(dtype, KIND_SMALL, K);
-      tiles = ((comp_elems >> K) + 255) / 256;
-    } else if (f == 0) {
-      e = find_kernel(dtype, KIND_ROW, K);
-      tiles = (comp_elems + (1ll << e->TB) - 1) >> e->TB;
-    } else {
-      e = find_kernel(dtype, KIND_COL, K, plan.col_bytes);
-      tiles = comp_elems >> e->TB;
+
+  // L2 chunking (opt-in): a multi-pass transform runs all its passes on one
+  // group of vectors before the next, so the intermediate written by a pass can
+  // be read back from L2 by the next one.  A group is as many whole vectors as
+  // fit the chunk budget; both parts share a launch when a vector pair fits, else
+  // the parts are chunked one at a time.  On GB300 the extra, smaller launches
+  // cost more than the L2 reuse saves for the specified workloads, so it is off
+  // by default.
+  const int ncomp_all = has_im ? 2 : 1;
+  const long long vec_bytes = (long long)esz << n;
+  const long long budget = chunk_budget();
+  long long vpc = batch;  // vectors per chunk
+  int parts_per_launch = ncomp_all;
+  bool chunked = false;
+  if (plan.nf >= 2 && budget > 0) {
+    if ((long long)ncomp_all * vec_bytes <= budget) {
+      vpc = std::max(1ll, budget / (ncomp_all * vec_bytes));
+    } else if (vec_bytes <= budget) {
+      parts_per_launch = 1;
+      vpc = std::max(1ll, budget / vec_bytes);
     }
-    if (tiles > INT_MAX) return FWT_ERR_UNSUPPORTED;
-    p.in[0] = f == 0 ? re_in : re_out;
-    p.in[1] = f == 0 ? im_in : im_out;
-    p.out[0] = re_out;
-    p.out[1] = im_out;
-    p.stride_log = L;
-    p.do_scale = (normalize && f == plan.nf - 1) ? 1 : 0;
-    const bool traced = g_trace_count + 2 <= g_trace_capacity;
-    if (traced) {
-      err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count], stream);
-      if (err != cudaSuccess) {
-        g_last_cuda_error = (int)err;
-        return FWT_ERR_CUDA;
+    chunked = vpc < batch || parts_per_launch < ncomp_all;
+  }
+  const void* ins[2] = {re_in, im_in};
+  void* outs[2] = {re_out, im_out};
+  for (int part0 = 0; part0 < ncomp_all; part0 += parts_per_launch) {
+    for (long long v0 = 0; v0 < batch; v0 += vpc) {
+      const long long nv = std::min(vpc, batch - v0);
+      const long long off = (v0 << n) * esz;  // byte offset of the chunk
+      const long long elems = nv << n;
+      int L = 0;
+      for (int f = 0; f < plan.nf; ++f) {
+        const int K = plan.bits[f];
+        const KernelEntry* e;
+        long long tiles;
+        if (f == 0 && K <= 2) {
+          e = find_kernel(dtype, KIND_SMALL, K);
+          tiles = ((elems >> K) + 255) / 256;
+        } else if (f == 0) {
+          e = find_kernel(dtype, KIND_ROW, K);
+          tiles = (elems + (1ll << e->TB) - 1) >> e->TB;
+        } else {
+          e = find_kernel(dtype, KIND_COL, K, plan.col_bytes);
+          tiles = elems >> e->TB;
+        }
+        if (tiles > INT_MAX) return FWT_ERR_UNSUPPORTED;
+        p.comp_elems = elems;
+        for (int c = 0; c < 2; ++c) {
+          const int part = part0 + (c < parts_per_launch ? c : 0);
+          const char* src = (const char*)(f == 0 ? ins[part] : outs[part]);
+          p.in[c] = src ? src + off : nullptr;
+          p.out[c] = outs[part] ? (char*)outs[part] + off : nullptr;
+        }
+        p.stride_log = L;
+        const bool last = f == plan.nf - 1;
+        p.do_scale = (normalize && last) ? 1 : 0;
+        p.ld_policy = 1;                          // read once
+        p.st_policy = last ? 1 : (chunked ? 2 : 0);  // keep intermediates for the next pass
+        const bool traced = g_trace_count + 2 <= g_trace_capacity;
+        if (traced) {
+          err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count], stream);
+          if (err != cudaSuccess) {
+            g_last_cuda_error = (int)err;
+            return FWT_ERR_CUDA;
+          }
+        }
+        err = e->launch(p, tiles, parts_per_launch, stream);
+        if (err == cudaSuccess && traced) {
+          err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count + 1], stream);
+          g_trace_count += 2;
+        }
+        if (err != cudaSuccess) {
+          g_last_cuda_error = (int)err;
+          return FWT_ERR_CUDA;
+        }
+        L += K;
       }
     }
-    err = e->launch(p, tiles, ncomp, stream);
-    if (err == cudaSuccess && traced) {
-      err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count + 1], stream);
-      g_trace_count += 2;
-    }
-    if (err != cudaSuccess) {
-      g_last_cuda_error = (int)err;
-      return FWT_ERR_CUDA;
-    }
-    L += K;
   }
   return FWT_OK;
 }
@@ -324,6 +375,18 @@ int fwt_get_column_bytes(int dtype) {
   if (dtype < 0 || dtype > 2) return -1;
   std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
   return fwt::g_col_bytes[dtype];
+}
+
+int fwt_set_l2_chunk_bytes(long long bytes) {
+  if (bytes < -1) return FWT_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(fwt::g_dev_mu);
+  fwt::g_chunk_bytes = bytes;
+  return FWT_OK;
+}
+
+long long fwt_get_l2_chunk_bytes(void) {
+  std::lock_guard<std::mutex> lk(fwt::g_dev_mu);
+  return fwt::g_chunk_bytes;
 }
 
 int fwt_trace_events(void** events, int capacity) {

@@ -47,6 +47,8 @@ struct PassParams {
   int scale_exp;         // fixed point: floor(-n/2) as a binary exponent
   int scale_half;        // fixed point: n odd, also divide by sqrt(2)
   unsigned long long rsqrt2_q64;  // floor(2^64 / sqrt(2))
+  int ld_policy;         // L2 eviction priority of the loads: 0 normal, 1 first, 2 last
+  int st_policy;         // ... and of the stores
 };
 
 // ---- arithmetic policies ----------------------------------------------------------
@@ -72,20 +74,32 @@ struct ArithI64 {  // magnitudes stay below 2^62 by construction; no wrap occurs
 };
 
 // ---- global memory access -------------------------------------------------------
+// Every load and store carries an L2 eviction-priority policy chosen per pass: the
+// input of a transform is read once (evict first), an intermediate that the next
+// pass reads back from L2 is kept (evict last), and the final result streams out
+// (evict first).
+__device__ __forceinline__ unsigned long long l2_policy(int kind) {
+  unsigned long long pol;
+  if (kind == 1) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  else if (kind == 2) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  else asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 template <typename U>
-__device__ __forceinline__ typename Vec16<U>::type ldg16(const void* p) {
+__device__ __forceinline__ typename Vec16<U>::type ldg16(const void* p, unsigned long long pol) {
   using V = typename Vec16<U>::type;
   uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+               : "l"(p), "l"(pol));
   return *reinterpret_cast<V*>(&v);
 }
 template <typename U>
-__device__ __forceinline__ void stg16(void* p, const typename Vec16<U>::type& val) {
+__device__ __forceinline__ void stg16(void* p, const typename Vec16<U>::type& val,
+                                      unsigned long long pol) {
   const uint4 v = *reinterpret_cast<const uint4*>(&val);
-  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
                : "memory");
 }
 
@@ -125,14 +139,16 @@ struct TileMap {
 };
 
 template <class S, bool COLS, typename T, typename U>
-__device__ __forceinline__ void load_tile(const T* in, const TileMap<S, COLS>& m, U (&x)[S::NE]) {
+__device__ __forceinline__ void load_tile(const T* in, const TileMap<S, COLS>& m, U (&x)[S::NE],
+                                          int policy) {
   using V = typename Vec16<U>::type;
   const uint32_t t = threadIdx.x;
+  const unsigned long long pol = l2_policy(policy);
 #pragma unroll
   for (int j = 0; j < S::NV; ++j) {
     const uint32_t u = S::idx1(t, j * S::VEC);
     V v;
-    if (m.in_range(u)) v = ldg16<U>(in + m.off(u));
+    if (m.in_range(u)) v = ldg16<U>(in + m.off(u), pol);
     else v = V{};
     const U* pv = reinterpret_cast<const U*>(&v);
 #pragma unroll
@@ -141,9 +157,11 @@ __device__ __forceinline__ void load_tile(const T* in, const TileMap<S, COLS>& m
 }
 
 template <class S, bool COLS, typename T, typename U>
-__device__ __forceinline__ void store_tile(T* out, const TileMap<S, COLS>& m, const U (&x)[S::NE]) {
+__device__ __forceinline__ void store_tile(T* out, const TileMap<S, COLS>& m, const U (&x)[S::NE],
+                                           int policy) {
   using V = typename Vec16<U>::type;
   const uint32_t t = threadIdx.x;
+  const unsigned long long pol = l2_policy(policy);
 #pragma unroll
   for (int j = 0; j < S::NV; ++j) {
     const uint32_t u = S::idx3(t, j * S::VEC);
@@ -151,7 +169,7 @@ __device__ __forceinline__ void store_tile(T* out, const TileMap<S, COLS>& m, co
     U* pv = reinterpret_cast<U*>(&v);
 #pragma unroll
     for (int i = 0; i < S::VEC; ++i) pv[i] = x[j * S::VEC + i];
-    if (m.in_range(u)) stg16<U>(out + m.off(u), v);
+    if (m.in_range(u)) stg16<U>(out + m.off(u), v, pol);
   }
 }
 
@@ -163,7 +181,7 @@ __device__ __forceinline__ void plain_tile(const PassParams& p, unsigned char* s
   T* out = static_cast<T*>(im ? p.out[1] : p.out[0]);
   const auto m = TileMap<S, COLS>::make(p, (long long)blockIdx.x);
   T x[S::NE];
-  load_tile<S, COLS>(in, m, x);
+  load_tile<S, COLS>(in, m, x, p.ld_policy);
   tile_rounds<S, A>(x, reinterpret_cast<T*>(smem_raw));
   if (p.do_scale) {
     if constexpr (sizeof(T) == 4 && !std::is_integral<T>::value) {
@@ -174,7 +192,7 @@ __device__ __forceinline__ void plain_tile(const PassParams& p, unsigned char* s
       for (int r = 0; r < S::NE; ++r) x[r] = x[r] * p.scale_f64;
     }
   }
-  store_tile<S, COLS>(out, m, x);
+  store_tile<S, COLS>(out, m, x, p.st_policy);
 }
 
 // ---- fp64 in exact 64-bit fixed point -------------------------------------------
@@ -272,7 +290,7 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
   double* out = static_cast<double*>(im ? p.out[1] : p.out[0]);
   const auto m = TileMap<S, COLS>::make(p, (long long)blockIdx.x);
   long long x[S::NE];
-  load_tile<S, COLS>(reinterpret_cast<const long long*>(in), m, x);
+  load_tile<S, COLS>(reinterpret_cast<const long long*>(in), m, x, p.ld_policy);
   // tile-wide largest exponent (and whether any Inf/NaN is present)
   uint32_t key = 0;
 #pragma unroll
@@ -292,7 +310,7 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
 #pragma unroll
       for (int r = 0; r < S::NE; ++r) xd[r] = xd[r] * p.scale_f64;
     }
-    store_tile<S, COLS>(out, m, xd);
+    store_tile<S, COLS>(out, m, xd, p.st_policy);
     return;
   }
   const int emax = max((int)(key >> 20), 1);  // zeros and subnormals scale as exponent 1
@@ -312,7 +330,7 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
 #pragma unroll
     for (int r = 0; r < S::NE; ++r) x[r] = from_fixed_exact(x[r], e0, half, p.rsqrt2_q64);
   }
-  store_tile<S, COLS>(reinterpret_cast<long long*>(out), m, x);
+  store_tile<S, COLS>(reinterpret_cast<long long*>(out), m, x, p.st_policy);
 }
 
 // ---- kernels --------------------------------------------------------------------
