@@ -301,7 +301,7 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
   key = red[0];
 #pragma unroll
   for (int w = 1; w < S::NT / 32; ++w) key = max(key, red[w]);
-  if (key >= 0x7ff00000u) {  // IEEE path for tiles with Inf/NaN
+  if (key >= 0x7ff00000u) {  // rare: a tile with Inf/NaN takes plain IEEE fp64 adds
     double xd[S::NE];
 #pragma unroll
     for (int r = 0; r < S::NE; ++r) xd[r] = __longlong_as_double(x[r]);
@@ -326,9 +326,14 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
     const long long e0_field = (long long)((unsigned long long)(long long)e0 << 52);
 #pragma unroll
     for (int r = 0; r < S::NE; ++r) x[r] = from_fixed_cvt(x[r], e0_field, half, p.rsqrt2_q64);
-  } else {
+  } else {  // rare: a rolled loop over a local copy keeps this code small
+    long long xl[S::NE];
 #pragma unroll
-    for (int r = 0; r < S::NE; ++r) x[r] = from_fixed_exact(x[r], e0, half, p.rsqrt2_q64);
+    for (int r = 0; r < S::NE; ++r) xl[r] = x[r];
+#pragma unroll 1
+    for (int r = 0; r < S::NE; ++r) xl[r] = from_fixed_exact(xl[r], e0, half, p.rsqrt2_q64);
+#pragma unroll
+    for (int r = 0; r < S::NE; ++r) x[r] = xl[r];
   }
   store_tile<S, COLS>(reinterpret_cast<long long*>(out), m, x, p.st_policy);
 }
