@@ -55,7 +55,7 @@ enum fwt_status {
   FWT_ERR_MISALIGNED = 2,  /* a pointer is not 16-byte aligned */
   FWT_ERR_UNSUPPORTED = 3, /* e.g. normalize with int32, or a plan the build lacks */
   FWT_ERR_CUDA = 4,        /* a CUDA call failed; see fwt_last_cuda_error() */
-  FWT_ERR_TIMEOUT = 5      /* reserved: a bounded device wait gave up */
+  FWT_ERR_TIMEOUT = 5      /* a bounded device wait gave up (see fwt_device_status) */
 };
 
 enum fwt_dtype { FWT_C32 = 0, FWT_C64 = 1, FWT_I32 = 2 };
@@ -129,6 +129,24 @@ int fwt_set_plan(int n, int dtype, int nfactors, const int* bits);
  */
 int fwt_set_column_bytes(int dtype, int bytes);
 int fwt_get_column_bytes(int dtype);
+
+/*
+ * How column passes move their strided tiles: mode 2 stages every tile through
+ * shared memory with TMA (cp.async.bulk.tensor) copies, 0 uses 16-byte vector
+ * loads and stores, 1 (default) uses TMA for column factors of 10 or more bits
+ * (tiles of 1024+ rows) and vector loads below.  All modes give identical
+ * results.  Affects default plans and plans set afterwards.  Returns FWT_OK or
+ * FWT_ERR_INVALID_ARG; fwt_get_tma returns the mode.
+ */
+int fwt_set_tma(int mode);
+int fwt_get_tma(void);
+
+/*
+ * Device-side status: returns FWT_ERR_TIMEOUT if, since the last call, some kernel
+ * gave up a bounded wait for a TMA copy (that tile was left unwritten), else
+ * FWT_OK; clears the record.  Synchronises the device (it reads device memory).
+ */
+int fwt_device_status(void);
 
 /*
  * L2 chunking of multi-pass transforms (tuning): when a plan has two or more

@@ -136,3 +136,12 @@ def test_l2_chunk_setting(lib):
     fwt.set_l2_chunk_bytes(0)
     with pytest.raises(fwt.FwtError):
         fwt.set_l2_chunk_bytes(-2)
+
+
+def test_tma_setting(lib):
+    assert fwt.tma() == fwt.TMA_AUTO
+    fwt.set_tma(fwt.TMA_NEVER)
+    assert fwt.tma() == fwt.TMA_NEVER
+    with pytest.raises(fwt.FwtError):
+        fwt.set_tma(3)
+    fwt.set_tma(fwt.TMA_AUTO)

@@ -65,22 +65,31 @@ def _valid_plans(n, dtype):
     return out
 
 
+@pytest.mark.parametrize("tma", [2, 0], ids=["tma", "direct"])
 @pytest.mark.parametrize("dtype", ["c32", "c64", "i32"])
 @pytest.mark.parametrize("n", [16, 20, 21])
-def test_every_kronecker_split(dtype, n):
-    """Each valid 2- and 3-factor split (every row and column tile shape) matches."""
-    plans = _valid_plans(n, dtype)
-    assert plans, "no valid plan"
+def test_every_kronecker_split(dtype, n, tma):
+    """Each valid 2- and 3-factor split, for every column segment width, with
+    TMA-staged and directly loaded column tiles (every compiled tile shape)."""
     re, im = inputs.random_pair(n, 2, dtype, seed=n)
     norm = dtype != "i32"
     ore, oim = oracle.fwt_complex(re, im, normalize=norm)
+    width = fwt.column_bytes(dtype)
+    fwt.set_tma(tma)
     try:
-        for f in plans:
-            fwt.set_plan(n, dtype, f)
-            gre, gim = gpu_transform(re, im, norm)
-            assert_matches(dtype, gre, gim, ore, oim, f"plan {f}")
+        for cb in ((32, 64, 128) if dtype == "c64" else (64, 128)):
+            fwt.set_column_bytes(dtype, cb)
+            plans = _valid_plans(n, dtype)
+            assert plans, "no valid plan"
+            for f in plans:
+                fwt.set_plan(n, dtype, f)
+                gre, gim = gpu_transform(re, im, norm)
+                assert_matches(dtype, gre, gim, ore, oim, f"plan {f} cb={cb} tma={tma}")
     finally:
         fwt.set_plan(n, dtype, None)
+        fwt.set_column_bytes(dtype, width)
+        fwt.set_tma(fwt.TMA_AUTO)
+    assert fwt.device_status() == fwt.FWT_OK
 
 
 @pytest.mark.parametrize("name", ["n10_b64_c32", "n12_b64_c32", "n14_b64_c32", "n18_b256_i32"])

@@ -70,6 +70,12 @@ def library() -> ctypes.CDLL:
         lib.fwt_set_column_bytes.restype = ci
         lib.fwt_get_column_bytes.argtypes = [ci]
         lib.fwt_get_column_bytes.restype = ci
+        lib.fwt_set_tma.argtypes = [ci]
+        lib.fwt_set_tma.restype = ci
+        lib.fwt_get_tma.argtypes = []
+        lib.fwt_get_tma.restype = ci
+        lib.fwt_device_status.argtypes = []
+        lib.fwt_device_status.restype = ci
         lib.fwt_set_l2_chunk_bytes.argtypes = [ctypes.c_longlong]
         lib.fwt_set_l2_chunk_bytes.restype = ci
         lib.fwt_get_l2_chunk_bytes.argtypes = []
@@ -134,6 +140,25 @@ def set_column_bytes(dtype: str, nbytes: int) -> None:
 
 def column_bytes(dtype: str) -> int:
     return library().fwt_get_column_bytes(DTYPES[dtype])
+
+
+TMA_NEVER, TMA_AUTO, TMA_ALWAYS = 0, 1, 2
+
+
+def set_tma(mode: int) -> None:
+    """Column-pass staging: TMA_ALWAYS, TMA_NEVER (vector loads) or TMA_AUTO (default)."""
+    st = library().fwt_set_tma(int(mode))
+    if st != FWT_OK:
+        raise FwtError(st, f"fwt_set_tma({mode})")
+
+
+def tma() -> int:
+    return library().fwt_get_tma()
+
+
+def device_status() -> int:
+    """FWT_ERR_TIMEOUT if a kernel gave up a bounded TMA wait since the last call."""
+    return library().fwt_device_status()
 
 
 def set_l2_chunk_bytes(nbytes: int) -> None:

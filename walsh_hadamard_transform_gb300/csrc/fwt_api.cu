@@ -34,9 +34,10 @@ const std::vector<KernelEntry>& table() {
   return t;
 }
 
-const KernelEntry* find_kernel(int dtype, int kind, int K, int col_bytes = 0) {
+const KernelEntry* find_kernel(int dtype, int kind, int K, int col_bytes = 0, int tma = 0) {
   for (const KernelEntry& e : table())
-    if (e.dtype == dtype && e.kind == kind && e.K == K && (kind != KIND_COL || e.col_bytes == col_bytes))
+    if (e.dtype == dtype && e.kind == kind && e.K == K &&
+        (kind != KIND_COL || (e.col_bytes == col_bytes && e.tma == tma)))
       return &e;
   return nullptr;
 }
@@ -51,11 +52,17 @@ struct Plan {
   int nf = 0;
   int bits[3] = {0, 0, 0};
   int col_bytes = 128;  // width of the column passes' row segments
+  int tma = 1;          // TMA-staged column passes: 0 never, 1 for K >= 10, 2 always
 };
+
+// TMA staging pays for column tiles with many rows (long strided walks); short
+// tiles are faster with plain vector loads (measured on GB300).
+int col_tma(const Plan& p, int K) { return p.tma == 2 || (p.tma == 1 && K >= 10) ? 1 : 0; }
 
 std::mutex g_plan_mu;
 Plan g_override[3][31];  // nf == 0: no override
 int g_col_bytes[3] = {64, 32, 64};  // default column segment width per dtype
+int g_use_tma = 1;                    // TMA-staged column passes: 0 never, 1 auto, 2 always
 
 int max_row_bits(int dtype) { return dtype == FWT_C64 ? 14 : 15; }
 // column factors available for a segment width: tiles of 2^10 .. 2^15 (2^14 fp64) elements
@@ -76,7 +83,7 @@ bool plan_valid(int n, int dtype, const Plan& p) {
         return false;
       }
     } else {
-      const KernelEntry* e = find_kernel(dtype, KIND_COL, k, p.col_bytes);
+      const KernelEntry* e = find_kernel(dtype, KIND_COL, k, p.col_bytes, col_tma(p, k));
       if (!e) return false;
       if (sum < e->TS) return false;  // a column segment must fit in one row
     }
@@ -90,6 +97,7 @@ Plan default_plan(int n, int dtype) {
   {
     std::lock_guard<std::mutex> lk(g_plan_mu);
     p.col_bytes = g_col_bytes[dtype];
+    p.tma = g_use_tma;
   }
   const int rmax = max_row_bits(dtype), cmin = min_col_bits(dtype, p.col_bytes),
             cmax = max_col_bits(dtype, p.col_bytes);
@@ -161,6 +169,9 @@ cudaError_t ensure_device() {
   return cudaSuccess;
 }
 
+std::once_flag g_encoder_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encoder = nullptr;
+
 // floor(2^64 / sqrt(2)) = floor(sqrt(2^127)), by bitwise integer square root.
 unsigned long long rsqrt2_q64() {
   const unsigned __int128 target = (unsigned __int128)1 << 127;
@@ -202,7 +213,7 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
         overlaps(im_out, re_in, bytes))
       return FWT_ERR_INVALID_ARG;
   }
-  const Plan plan = get_plan(n, dtype);
+  Plan plan = get_plan(n, dtype);
   if (!plan_valid(n, dtype, plan)) return FWT_ERR_UNSUPPORTED;
 
   cudaError_t err = ensure_device();
@@ -210,6 +221,7 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
     g_last_cuda_error = (int)err;
     return FWT_ERR_CUDA;
   }
+  if (plan.tma && !tensor_map_encoder()) plan.tma = 0;  // driver without the TMA encoder
 
   PassParams p{};
   const double s = n % 2 == 0 ? std::ldexp(1.0, -n / 2) : std::ldexp(1.0, -(n - 1) / 2) / std::sqrt(2.0);
@@ -260,7 +272,7 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
           e = find_kernel(dtype, KIND_ROW, K);
           tiles = (elems + (1ll << e->TB) - 1) >> e->TB;
         } else {
-          e = find_kernel(dtype, KIND_COL, K, plan.col_bytes);
+          e = find_kernel(dtype, KIND_COL, K, plan.col_bytes, col_tma(plan, K));
           tiles = elems >> e->TB;
         }
         if (tiles > INT_MAX) return FWT_ERR_UNSUPPORTED;
@@ -301,6 +313,19 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
 }
 
 }  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  std::call_once(g_encoder_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encoder = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encoder;
+}
+
 }  // namespace fwt
 
 extern "C" {
@@ -351,6 +376,7 @@ int fwt_set_plan(int n, int dtype, int nfactors, const int* bits) {
   {
     std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
     p.col_bytes = fwt::g_col_bytes[dtype];
+    p.tma = fwt::g_use_tma;
   }
   for (int f = 0; f < nfactors; ++f) {
     if (!bits) return FWT_ERR_INVALID_ARG;
@@ -375,6 +401,30 @@ int fwt_get_column_bytes(int dtype) {
   if (dtype < 0 || dtype > 2) return -1;
   std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
   return fwt::g_col_bytes[dtype];
+}
+
+int fwt_set_tma(int mode) {
+  if (mode < 0 || mode > 2) return FWT_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
+  fwt::g_use_tma = mode;
+  return FWT_OK;
+}
+
+int fwt_get_tma(void) {
+  std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
+  return fwt::g_use_tma;
+}
+
+int fwt_device_status(void) {
+  unsigned int e[3] = {0, 0, 0};
+  cudaError_t err = fwt::read_device_error_c32(&e[0]);
+  if (err == cudaSuccess) err = fwt::read_device_error_c64(&e[1]);
+  if (err == cudaSuccess) err = fwt::read_device_error_i32(&e[2]);
+  if (err != cudaSuccess) {
+    fwt::g_last_cuda_error = (int)err;
+    return FWT_ERR_CUDA;
+  }
+  return (e[0] | e[1] | e[2]) ? FWT_ERR_TIMEOUT : FWT_OK;
 }
 
 int fwt_set_l2_chunk_bytes(long long bytes) {

@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 
 #include "tile_engine.cuh"
+#include "tma.cuh"
 
 namespace fwt {
 
@@ -173,15 +174,100 @@ __device__ __forceinline__ void store_tile(T* out, const TileMap<S, COLS>& m, co
   }
 }
 
+// ---- tile movers: HBM <-> registers ----------------------------------------------
+// Direct: 16-byte vector loads into layout L1, stores from layout L3.
+template <class S, bool COLS>
+struct DirectMover {
+  TileMap<S, COLS> m;
+  const void* in;
+  void* out;
+  __device__ DirectMover(const PassParams& p, unsigned char*) {
+    const bool im = blockIdx.y != 0;
+    in = im ? p.in[1] : p.in[0];
+    out = im ? p.out[1] : p.out[0];
+    m = TileMap<S, COLS>::make(p, (long long)blockIdx.x);
+  }
+  template <typename U>
+  __device__ __forceinline__ bool load(U (&x)[S::NE], int policy) {
+    load_tile<S, COLS>(static_cast<const U*>(in), m, x, policy);
+    return true;
+  }
+  template <typename U>
+  __device__ __forceinline__ void store(const U (&x)[S::NE], int policy) {
+    store_tile<S, COLS>(static_cast<U*>(out), m, x, policy);
+  }
+};
+
+// Parameters of a TMA column pass: one tensor map per part (rows of 2^L
+// elements, box of CW columns x up to 256 rows), then the common parameters.
+struct TmaPassParams {
+  CUtensorMap map[2];
+  PassParams p;
+};
+
+// TMA: the column tile arrives in shared memory in natural order; threads pick up
+// layout L1 there, and write layout L3 back there for a TMA store.
+template <class S>
+struct TmaMover {
+  static constexpr int BOXR = S::TK >= 8 ? 256 : (1 << S::TK);  // rows per copy
+  static constexpr int NBOX = (1 << S::TK) / BOXR;
+  static constexpr uint32_t BOX_ELEMS = (uint32_t)BOXR << S::TS;
+  const CUtensorMap* map;
+  int col0, row0;
+  unsigned char* smem;
+  uint64_t* bar;
+  __device__ TmaMover(const TmaPassParams& tp, unsigned char* smem_raw, uint64_t* barrier) {
+    const bool im = blockIdx.y != 0;
+    map = im ? &tp.map[1] : &tp.map[0];
+    const int chunks_lg = tp.p.stride_log - S::TS;
+    const long long tile = blockIdx.x;
+    col0 = (int)((tile & ((1ll << chunks_lg) - 1)) << S::TS);
+    row0 = (int)((tile >> chunks_lg) << S::TK);
+    smem = smem_raw;
+    bar = barrier;
+    if (threadIdx.x == 0) mbar_init(bar, 1);
+    __syncthreads();
+  }
+  template <typename U>
+  __device__ __forceinline__ bool load(U (&x)[S::NE], int policy) {
+    if (threadIdx.x == 0) {
+      const unsigned long long pol = l2_policy(policy);
+      mbar_arrive_expect_tx(bar, (uint32_t)(sizeof(U) << S::TB));
+#pragma unroll
+      for (int i = 0; i < NBOX; ++i)
+        tma_load_2d(smem + (size_t)i * BOX_ELEMS * sizeof(U), map, col0, row0 + i * BOXR, bar, pol);
+    }
+    const bool ok = mbar_wait_bounded(bar, 0);
+    if (__syncthreads_or(!ok)) return false;  // the whole tile is skipped
+    const U* sm = reinterpret_cast<const U*>(smem);
+#pragma unroll
+    for (int j = 0; j < S::NV; ++j) get_vec<U, S::VEC>(sm + S::idx1(threadIdx.x, j * S::VEC), x, j);
+    __syncthreads();  // the tile engine reuses the buffer
+    return true;
+  }
+  template <typename U>
+  __device__ __forceinline__ void store(const U (&x)[S::NE], int policy) {
+    U* sm = reinterpret_cast<U*>(smem);
+    __syncthreads();  // the engine's last reads of the buffer are done
+#pragma unroll
+    for (int j = 0; j < S::NV; ++j) put_vec<U, S::VEC>(sm + S::idx3(threadIdx.x, j * S::VEC), x, j);
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const unsigned long long pol = l2_policy(policy);
+#pragma unroll
+      for (int i = 0; i < NBOX; ++i)
+        tma_store_2d(map, col0, row0 + i * BOXR, smem + (size_t)i * BOX_ELEMS * sizeof(U), pol);
+      tma_store_commit_and_wait();
+    }
+  }
+};
+
 // ---- fp32 / int32 / plain fp64 tile ---------------------------------------------
-template <class S, class A, bool COLS, typename T>
-__device__ __forceinline__ void plain_tile(const PassParams& p, unsigned char* smem_raw) {
-  const bool im = blockIdx.y != 0;
-  const T* in = static_cast<const T*>(im ? p.in[1] : p.in[0]);
-  T* out = static_cast<T*>(im ? p.out[1] : p.out[0]);
-  const auto m = TileMap<S, COLS>::make(p, (long long)blockIdx.x);
+template <class S, class A, typename T, class Mover>
+__device__ __forceinline__ void plain_tile(const PassParams& p, unsigned char* smem_raw, Mover& mv) {
   T x[S::NE];
-  load_tile<S, COLS>(in, m, x, p.ld_policy);
+  if (!mv.load(x, p.ld_policy)) return;
   tile_rounds<S, A>(x, reinterpret_cast<T*>(smem_raw));
   if (p.do_scale) {
     if constexpr (sizeof(T) == 4 && !std::is_integral<T>::value) {
@@ -192,7 +278,7 @@ __device__ __forceinline__ void plain_tile(const PassParams& p, unsigned char* s
       for (int r = 0; r < S::NE; ++r) x[r] = x[r] * p.scale_f64;
     }
   }
-  store_tile<S, COLS>(out, m, x, p.st_policy);
+  mv.store(x, p.st_policy);
 }
 
 // ---- fp64 in exact 64-bit fixed point -------------------------------------------
@@ -282,15 +368,11 @@ __device__ __forceinline__ long long from_fixed_cvt(long long q, long long e0_fi
   return q == 0 ? 0ll : b + e0_field;
 }
 
-template <class S, bool COLS>
-__device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* smem_raw) {
+template <class S, class Mover>
+__device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* smem_raw, Mover& mv) {
   __shared__ uint32_t red[32];
-  const bool im = blockIdx.y != 0;
-  const double* in = static_cast<const double*>(im ? p.in[1] : p.in[0]);
-  double* out = static_cast<double*>(im ? p.out[1] : p.out[0]);
-  const auto m = TileMap<S, COLS>::make(p, (long long)blockIdx.x);
   long long x[S::NE];
-  load_tile<S, COLS>(reinterpret_cast<const long long*>(in), m, x, p.ld_policy);
+  if (!mv.load(x, p.ld_policy)) return;
   // tile-wide largest exponent (and whether any Inf/NaN is present)
   uint32_t key = 0;
 #pragma unroll
@@ -310,7 +392,7 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
 #pragma unroll
       for (int r = 0; r < S::NE; ++r) xd[r] = xd[r] * p.scale_f64;
     }
-    store_tile<S, COLS>(out, m, xd, p.st_policy);
+    mv.store(xd, p.st_policy);
     return;
   }
   const int emax = max((int)(key >> 20), 1);  // zeros and subnormals scale as exponent 1
@@ -335,19 +417,35 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
 #pragma unroll
     for (int r = 0; r < S::NE; ++r) x[r] = xl[r];
   }
-  store_tile<S, COLS>(reinterpret_cast<long long*>(out), m, x, p.st_policy);
+  mv.store(x, p.st_policy);
 }
 
 // ---- kernels --------------------------------------------------------------------
 // KIND: 0 = fp32, 1 = fp64 (fixed point), 2 = int32, 3 = fp64 plain IEEE
 // Two CTAs per SM for tiles up to 256 threads (at most 128 registers a thread).
+template <class S, int KIND, class Mover>
+__device__ __forceinline__ void tile_body(const PassParams& p, unsigned char* smem_raw, Mover& mv) {
+  if constexpr (KIND == 0) plain_tile<S, ArithF32, float>(p, smem_raw, mv);
+  else if constexpr (KIND == 1) fixed_tile<S>(p, smem_raw, mv);
+  else if constexpr (KIND == 2) plain_tile<S, ArithU32, uint32_t>(p, smem_raw, mv);
+  else plain_tile<S, ArithF64, double>(p, smem_raw, mv);
+}
+
 template <class S, int KIND, bool COLS>
 __global__ void __launch_bounds__(S::NT, S::NT <= 256 ? 2 : 1) fwt_tile_kernel(const PassParams p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  if constexpr (KIND == 0) plain_tile<S, ArithF32, COLS, float>(p, smem_raw);
-  else if constexpr (KIND == 1) fixed_tile<S, COLS>(p, smem_raw);
-  else if constexpr (KIND == 2) plain_tile<S, ArithU32, COLS, uint32_t>(p, smem_raw);
-  else plain_tile<S, ArithF64, COLS, double>(p, smem_raw);
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  DirectMover<S, COLS> mv(p, smem_raw);
+  tile_body<S, KIND>(p, smem_raw, mv);
+}
+
+// Column pass with TMA-staged tiles.
+template <class S, int KIND>
+__global__ void __launch_bounds__(S::NT, S::NT <= 256 ? 2 : 1)
+    fwt_col_tma_kernel(const __grid_constant__ TmaPassParams tp) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bar;
+  TmaMover<S> mv(tp, smem_raw, &bar);
+  tile_body<S, KIND>(tp.p, smem_raw, mv);
 }
 
 // Vectors of 2^NL <= 4 elements: one thread per vector, plain arithmetic.

@@ -8,9 +8,18 @@ template <int... Ks> void rows(std::vector<KernelEntry>& v, std::integer_sequenc
   (v.push_back(row_entry<FWT_I32, 2, 2, Ks + 3>()), ...);
 }
 template <int CB, int K0, int... Ks> void cols(std::vector<KernelEntry>& v, std::integer_sequence<int, Ks...>) {
-  (v.push_back(col_entry<FWT_I32, 2, 2, Ks + K0, CB>()), ...);
+  (v.push_back(col_entry<FWT_I32, 2, 2, Ks + K0, CB, false>()), ...);
+  (v.push_back(col_entry<FWT_I32, 2, 2, Ks + K0, CB, true>()), ...);
 }
 }  // namespace
+
+// Reads and clears this translation unit's device error word (synchronising).
+cudaError_t read_device_error_i32(unsigned int* out) {
+  unsigned int zero = 0;
+  cudaError_t err = cudaMemcpyFromSymbol(out, g_device_error, sizeof(unsigned int));
+  if (err == cudaSuccess && *out) err = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(unsigned int));
+  return err;
+}
 
 void register_i32(std::vector<KernelEntry>& v) {
   v.push_back(small_entry<FWT_I32, uint32_t, ArithU32, 0>());

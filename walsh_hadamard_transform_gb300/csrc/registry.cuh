@@ -6,6 +6,7 @@
 #include <vector>
 
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "fwt_kernels.cuh"
 
@@ -19,7 +20,8 @@ struct KernelEntry {
   int K;      // transformed index bits of the pass
   int TB;     // log2 elements per tile (0 for the small kernel)
   int TS;     // first transformed tile bit (column tiles: log2 columns per tile)
-  int col_bytes;  // column tiles: bytes of contiguous columns per row (64 or 128)
+  int col_bytes;  // column tiles: bytes of contiguous columns per row (32, 64 or 128)
+  int tma;        // column tiles staged through shared memory by TMA copies
   int threads;
   size_t smem;  // dynamic shared memory per CTA
   cudaError_t (*launch)(const PassParams&, long long tiles, int ncomp, cudaStream_t);
@@ -137,6 +139,19 @@ int check_shape(const char* name) {
       }
     }
   }
+  // 4c. TMA-staged column tiles: layout L1 reads and layout L3 writes of the
+  //     natural-order tile are conflict-free too
+  if (COLS) {
+    for (uint32_t w = 0; w < (uint32_t)S::NT / 32; ++w)
+      for (int j = 0; j < S::NV; ++j)
+        for (int layout = 1; layout <= 3; layout += 2) {
+          for (int l = 0; l < 32; ++l) addr[l] = host_idx<S>(layout, w * 32 + l, j * S::VEC) * esz;
+          if (smem_wavefronts(addr, 16) != 4) {
+            if (fails < 12) fprintf(stderr, "fwt_selfcheck %s: natural-order conflict layout %d\n", name, layout);
+            ++fails;
+          }
+        }
+  }
   // 5. global accesses: every warp-wide 16-byte load (L1) and store (L3) fills
   //    whole 32-byte sectors (row tiles: 512 contiguous bytes)
   const int L = COLS ? S::TS + 3 : 0;  // any row stride >= the column width
@@ -179,8 +194,47 @@ cudaError_t launch_small(const PassParams& p, long long tiles, int ncomp, cudaSt
   fwt_small_kernel<T, A, NL><<<dim3((unsigned)tiles, (unsigned)ncomp), 256, 0, st>>>(p);
   return cudaGetLastError();
 }
-inline cudaError_t setup_none() { return cudaSuccess; }
 inline int selfcheck_none() { return 0; }
+
+// The driver's tensor-map encoder, resolved once at run time (nullptr if absent).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+template <class S, int KIND>
+cudaError_t launch_col_tma(const PassParams& p, long long tiles, int ncomp, cudaStream_t st) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  constexpr int esz = (KIND == 1 || KIND == 3) ? 8 : 4;
+  const CUtensorMapDataType dt = esz == 8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT64
+                                 : KIND == 2 ? CU_TENSOR_MAP_DATA_TYPE_INT32
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const cuuint64_t rows = (cuuint64_t)(p.comp_elems >> p.stride_log);
+  if (rows > 0xffffffffull) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {1ull << p.stride_log, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)esz << p.stride_log};
+  const cuuint32_t box[2] = {1u << S::TS, (cuuint32_t)TmaMover<S>::BOXR};
+  const cuuint32_t estr[2] = {1, 1};
+  TmaPassParams tp;
+  tp.p = p;
+  for (int c = 0; c < ncomp; ++c) {
+    if (p.in[c] != p.out[c]) return cudaErrorInvalidValue;  // column passes run in place
+    const CUresult r = enc(&tp.map[c], dt, 2, p.out[c], dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  if (ncomp == 1) tp.map[1] = tp.map[0];
+  const size_t smem = (size_t)esz << S::TB;
+  fwt_col_tma_kernel<S, KIND><<<dim3((unsigned)tiles, (unsigned)ncomp), S::NT, smem, st>>>(tp);
+  return cudaGetLastError();
+}
+template <class S, int KIND>
+cudaError_t setup_col_tma() {
+  const size_t smem = (size_t)((KIND == 1 || KIND == 3) ? 8 : 4) << S::TB;
+  return cudaFuncSetAttribute(fwt_col_tma_kernel<S, KIND>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+inline cudaError_t setup_none() { return cudaSuccess; }
 
 // Row pass over bits [0, K): tiles of 2^max(K, 10) contiguous elements.
 template <int DT, int KIND, int LV, int K>
@@ -189,7 +243,7 @@ KernelEntry row_entry() {
   constexpr int EL = choose_el(TB, LV);
   using S = Shape<TB, 0, K, LV, TB - EL>;
   KernelEntry e;
-  e.dtype = DT; e.kind = KIND_ROW; e.K = K; e.TB = TB; e.TS = 0; e.col_bytes = 0;
+  e.dtype = DT; e.kind = KIND_ROW; e.K = K; e.TB = TB; e.TS = 0; e.col_bytes = 0; e.tma = 0;
   e.threads = S::NT;
   e.smem = (size_t)(1u << TB) * (16 >> LV);
   e.launch = &launch_tile<S, KIND, false>;
@@ -201,7 +255,7 @@ KernelEntry row_entry() {
 
 // Column pass over bits [L, L + K): tiles of 2^K rows x CB bytes of columns
 // (CB = 32, 64 or 128: two, four or eight 16-byte vectors).
-template <int DT, int KIND, int LV, int K, int CB>
+template <int DT, int KIND, int LV, int K, int CB, bool TMA>
 KernelEntry col_entry() {
   constexpr int CWL = LV + (CB == 128 ? 3 : CB == 64 ? 2 : 1);
   constexpr int TB = K + CWL;
@@ -209,19 +263,27 @@ KernelEntry col_entry() {
   using S = Shape<TB, CWL, K, LV, TB - EL>;
   KernelEntry e;
   e.dtype = DT; e.kind = KIND_COL; e.K = K; e.TB = TB; e.TS = CWL; e.col_bytes = CB;
+  e.tma = TMA ? 1 : 0;
   e.threads = S::NT;
   e.smem = (size_t)(1u << TB) * (16 >> LV);
-  e.launch = &launch_tile<S, KIND, true>;
-  e.setup = &setup_tile<S, KIND, true>;
-  e.selfcheck = [] { return check_shape<S, true>("col"); };
-  e.fn = (const void*)&fwt_tile_kernel<S, KIND, true>;
+  if constexpr (TMA) {
+    e.launch = &launch_col_tma<S, KIND>;
+    e.setup = &setup_col_tma<S, KIND>;
+    e.selfcheck = &selfcheck_none;  // same shape as the direct kernel, checked there
+    e.fn = (const void*)&fwt_col_tma_kernel<S, KIND>;
+  } else {
+    e.launch = &launch_tile<S, KIND, true>;
+    e.setup = &setup_tile<S, KIND, true>;
+    e.selfcheck = [] { return check_shape<S, true>("col"); };
+    e.fn = (const void*)&fwt_tile_kernel<S, KIND, true>;
+  }
   return e;
 }
 
 template <int DT, typename T, class A, int NL>
 KernelEntry small_entry() {
   KernelEntry e;
-  e.dtype = DT; e.kind = KIND_SMALL; e.K = NL; e.TB = 0; e.TS = 0; e.col_bytes = 0;
+  e.dtype = DT; e.kind = KIND_SMALL; e.K = NL; e.TB = 0; e.TS = 0; e.col_bytes = 0; e.tma = 0;
   e.threads = 256; e.smem = 0;
   e.launch = &launch_small<T, A, NL>;
   e.setup = &setup_none;
@@ -230,6 +292,9 @@ KernelEntry small_entry() {
   return e;
 }
 
+cudaError_t read_device_error_c32(unsigned int* out);
+cudaError_t read_device_error_c64(unsigned int* out);
+cudaError_t read_device_error_i32(unsigned int* out);
 void register_c32(std::vector<KernelEntry>& v);
 void register_c64(std::vector<KernelEntry>& v);
 void register_i32(std::vector<KernelEntry>& v);
