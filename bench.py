@@ -17,6 +17,7 @@ with no collective on the data path (weak scaling); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -53,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(STEP_WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the batch of every part (small cases for profiling; 0 = as specified)")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -231,6 +234,8 @@ def run_ours(args):
     fwt.library()
 
     parts = [inputs.WORKLOADS[name] for name in STEP_WORKLOADS[args.workload]]
+    if args.batch > 0:
+        parts = [dataclasses.replace(w, batch=args.batch) for w in parts]
     host, dev_in, dev_out = [], [], []
     for w in parts:
         re, im = inputs.draw(w.values, w.n, w.batch, rank_seed(w.seed, rank), w.dtype)
@@ -308,7 +313,7 @@ def run_ours(args):
         "dtype": "+".join(sorted({{"c64": "int64", "c32": "f32", "i32": "int32"}[w.dtype] for w in parts})),
         "data": "synthetic (seeded PCG64; Gaussian unit-L2 states / uniform ints, per the workload)",
         "config": {
-            "workload": args.workload,
+            "workload": args.workload if args.batch <= 0 else "%s (batch %d)" % (args.workload, args.batch),
             "parts": [{"name": w.name, "n": w.n, "batch": w.batch, "dtype": w.dtype,
                        "normalize": w.normalize, "factors": fwt.plan_factors(w.n, w.dtype)}
                       for w in parts],
