@@ -63,6 +63,12 @@ class Oracle:
         lib.oracle_fwt_f64.restype = ctypes.c_int
         lib.oracle_fwt_u32.argtypes = [up, up, ctypes.c_int, i64, ctypes.c_int]
         lib.oracle_fwt_u32.restype = ctypes.c_int
+        lib.oracle_fwt_bits_f64.argtypes = [dp, dp, ctypes.c_int, i64, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int]
+        lib.oracle_fwt_bits_f64.restype = ctypes.c_int
+        lib.oracle_fwt_bits_u32.argtypes = [up, up, ctypes.c_int, i64, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int]
+        lib.oracle_fwt_bits_u32.restype = ctypes.c_int
         lib.oracle_fwt_entry_f64.argtypes = [dp, ctypes.c_int, i64, ctypes.c_int]
         lib.oracle_fwt_entry_f64.restype = ctypes.c_double
         lib.oracle_fwt_entry_u32.argtypes = [up, ctypes.c_int, i64]
@@ -112,6 +118,34 @@ class Oracle:
             raise RuntimeError(f"oracle_fwt_f64 failed ({rc})")
         return out
 
+    def fwt_bits(self, x, lo: int, nbits: int, normalize: bool = True, nthreads: int = 1):
+        """Transform over index bits [lo, lo+nbits) of every row of ``x`` (last axis):
+        I (x) H_nbits (x) I_{2^lo}, scaled by 2^{-nbits/2} when normalising."""
+        x = np.asarray(x)
+        n = self._n_of(x.shape[-1])
+        count = x.size // x.shape[-1] if x.size else 0
+        if x.dtype in (np.int32, np.uint32):
+            if normalize:
+                raise ValueError("int32 transform has no normalised form")
+            src = np.ascontiguousarray(x).view(np.uint32)
+            out = np.empty_like(src)
+            rc = self.lib.oracle_fwt_bits_u32(
+                src.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)),
+                out.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)), n, count, int(lo), int(nbits),
+                int(nthreads))
+            if rc:
+                raise RuntimeError(f"oracle_fwt_bits_u32 failed ({rc})")
+            return out.view(np.int32)
+        src = np.ascontiguousarray(x, dtype=np.float64)
+        out = np.empty_like(src)
+        rc = self.lib.oracle_fwt_bits_f64(
+            src.ctypes.data_as(ctypes.POINTER(ctypes.c_double)),
+            out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), n, count, int(lo), int(nbits),
+            int(bool(normalize)), int(nthreads))
+        if rc:
+            raise RuntimeError(f"oracle_fwt_bits_f64 failed ({rc})")
+        return out
+
     def fwt_complex(self, re, im, normalize: bool = True, nthreads: int = 1):
         """H is real, so a split complex vector transforms component by component."""
         out_im = None if im is None else self.fwt(im, normalize, nthreads)
@@ -155,6 +189,10 @@ def fwt(x, normalize: bool = True, nthreads: int = 1) -> np.ndarray:
 
 def fwt_complex(re, im, normalize: bool = True, nthreads: int = 1):
     return default().fwt_complex(re, im, normalize, nthreads)
+
+
+def fwt_bits(x, lo: int, nbits: int, normalize: bool = True, nthreads: int = 1) -> np.ndarray:
+    return default().fwt_bits(x, lo, nbits, normalize, nthreads)
 
 
 def entry(vec, k: int, normalize: bool = True):

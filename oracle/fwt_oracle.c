@@ -12,13 +12,18 @@
  * fwt", section "How" (naive GEMM placeholder); the scale 2^{-n/2} is the usual
  * orthonormal scaling of H_n.
  *
- * Two routines:
+ * Routines:
  *   - oracle_fwt_f64 / oracle_fwt_u32: the textbook in-place butterfly network,
  *     stage h pairing entries at distance 1, 2, 4, ... with (a+b, a-b), as in the
  *     iThome "Day 18" FWT post, section "Tensor Core wants matrix
  *     multiplication" (stage 0 local pairs, stage 1 stride 2, stage 2 stride 4).
  *     Floating point runs in double; int32 runs in uint32_t so that overflow
  *     wraps modulo 2^32 (signed overflow is undefined in C).
+ *   - oracle_fwt_bits_f64 / oracle_fwt_bits_u32: the same network restricted to
+ *     the stages of index bits [lo, lo+nbits), i.e. I (x) H_nbits (x) I applied to
+ *     each vector (a transform on a subset of qubits; the Kronecker factors of
+ *     "[QDP] [feature] Pr4 kronecker fwt", deliverables: (H_{n1} (x) I) and
+ *     (I (x) H_{n2})).
  *   - oracle_fwt_entry_f64 / oracle_fwt_entry_u32: one output entry straight from
  *     the definition above, O(N) per entry, for spot checks at sizes where the
  *     whole reference transform is too slow to repeat.
@@ -37,6 +42,35 @@ double oracle_scale(int n, int normalize) {
   if (!normalize) return 1.0;
   if (n % 2 == 0) return ldexp(1.0, -n / 2);
   return ldexp(1.0, -(n - 1) / 2) / sqrt(2.0);
+}
+
+/* Stages h = 2^lo, 2^(lo+1), ..., 2^(lo+nbits-1) of the butterfly network: the
+ * transform over index bits [lo, lo+nbits) only, i.e. (I (x) H_nbits (x) I_{2^lo}) x.
+ * With lo = 0 and nbits = n it is the whole transform. */
+static void butterfly_bits_f64(double* x, int64_t N, int lo, int nbits) {
+  for (int64_t h = (int64_t)1 << lo; h < ((int64_t)1 << (lo + nbits)); h *= 2) {
+    for (int64_t i = 0; i < N; i += 2 * h) {
+      for (int64_t j = i; j < i + h; ++j) {
+        double u = x[j];
+        double v = x[j + h];
+        x[j] = u + v;
+        x[j + h] = u - v;
+      }
+    }
+  }
+}
+
+static void butterfly_bits_u32(uint32_t* x, int64_t N, int lo, int nbits) {
+  for (int64_t h = (int64_t)1 << lo; h < ((int64_t)1 << (lo + nbits)); h *= 2) {
+    for (int64_t i = 0; i < N; i += 2 * h) {
+      for (int64_t j = i; j < i + h; ++j) {
+        uint32_t u = x[j];
+        uint32_t v = x[j + h];
+        x[j] = u + v;
+        x[j + h] = u - v;
+      }
+    }
+  }
 }
 
 static void butterfly_f64(double* x, int64_t N) {
@@ -72,6 +106,7 @@ typedef struct {
   int64_t first, last; /* vectors [first, last) */
   double scale;
   int is_int;
+  int lo, nbits; /* nbits < 0: the whole transform */
 } job_t;
 
 static void* run_job(void* arg) {
@@ -82,12 +117,14 @@ static void* run_job(void* arg) {
       const uint32_t* src = (const uint32_t*)jb->x + b * N;
       uint32_t* dst = (uint32_t*)jb->y + b * N;
       if (dst != src) memcpy(dst, src, (size_t)N * sizeof(uint32_t));
-      butterfly_u32(dst, N);
+      if (jb->nbits < 0) butterfly_u32(dst, N);
+      else butterfly_bits_u32(dst, N, jb->lo, jb->nbits);
     } else {
       const double* src = (const double*)jb->x + b * N;
       double* dst = (double*)jb->y + b * N;
       if (dst != src) memcpy(dst, src, (size_t)N * sizeof(double));
-      butterfly_f64(dst, N);
+      if (jb->nbits < 0) butterfly_f64(dst, N);
+      else butterfly_bits_f64(dst, N, jb->lo, jb->nbits);
       if (jb->scale != 1.0)
         for (int64_t k = 0; k < N; ++k) dst[k] *= jb->scale;
     }
@@ -96,8 +133,9 @@ static void* run_job(void* arg) {
 }
 
 static int run_batch(const void* x, void* y, int n, int64_t count, double scale,
-                     int is_int, int nthreads) {
+                     int is_int, int nthreads, int lo, int nbits) {
   if (n < 0 || n > 40 || count < 0 || (count > 0 && (!x || !y))) return 1;
+  if (nbits >= 0 && (lo < 0 || lo + nbits > n)) return 1;
   if (nthreads < 1) nthreads = 1;
   if (nthreads > count) nthreads = count > 0 ? (int)count : 1;
   job_t* jobs = (job_t*)calloc((size_t)nthreads, sizeof(job_t));
@@ -106,6 +144,7 @@ static int run_batch(const void* x, void* y, int n, int64_t count, double scale,
   for (int t = 0; t < nthreads; ++t) {
     jobs[t].x = x; jobs[t].y = y; jobs[t].n = n; jobs[t].scale = scale;
     jobs[t].is_int = is_int;
+    jobs[t].lo = lo; jobs[t].nbits = nbits;
     jobs[t].first = count * t / nthreads;
     jobs[t].last = count * (t + 1) / nthreads;
   }
@@ -126,12 +165,26 @@ static int run_batch(const void* x, void* y, int n, int64_t count, double scale,
 /* count vectors of 2^n doubles, x -> y (y may equal x).  Returns 0 on success. */
 int oracle_fwt_f64(const double* x, double* y, int n, int64_t count, int normalize,
                    int nthreads) {
-  return run_batch(x, y, n, count, oracle_scale(n, normalize), 0, nthreads);
+  return run_batch(x, y, n, count, oracle_scale(n, normalize), 0, nthreads, 0, -1);
 }
 
 /* count vectors of 2^n uint32 (int32 bit patterns), wrap-around arithmetic. */
 int oracle_fwt_u32(const uint32_t* x, uint32_t* y, int n, int64_t count, int nthreads) {
-  return run_batch(x, y, n, count, 1.0, 1, nthreads);
+  return run_batch(x, y, n, count, 1.0, 1, nthreads, 0, -1);
+}
+
+/* The transform over index bits [lo, lo+nbits) of each 2^n vector (the other bits
+ * untouched), scaled by 2^{-nbits/2} when normalising. */
+int oracle_fwt_bits_f64(const double* x, double* y, int n, int64_t count, int lo, int nbits,
+                        int normalize, int nthreads) {
+  if (nbits < 0) return 1;
+  return run_batch(x, y, n, count, oracle_scale(nbits, normalize), 0, nthreads, lo, nbits);
+}
+
+int oracle_fwt_bits_u32(const uint32_t* x, uint32_t* y, int n, int64_t count, int lo, int nbits,
+                        int nthreads) {
+  if (nbits < 0) return 1;
+  return run_batch(x, y, n, count, 1.0, 1, nthreads, lo, nbits);
 }
 
 /* Parity of popc(v): XOR-fold the 64 bits down to one. */

@@ -196,6 +196,34 @@ def pin_fp32_promotion(orc):
     assert np.array_equal(orc.fwt(x, normalize=True), orc.fwt(x.astype(np.float64), normalize=True))
 
 
+def pin_bit_range(orc):
+    """The transform over index bits [lo, lo+k): I (x) H_k (x) I_{2^lo} (dense Kronecker
+    product of popc matrices), the whole transform for [0, n), and a partition of
+    [0, n) into ranges composes to the whole transform."""
+    rng = np.random.default_rng(23)
+    for n in (1, 3, 6, 9):
+        x = rng.standard_normal((2, 1 << n))
+        xi = rng.integers(-(2 ** 31), 2 ** 31, size=(2, 1 << n), dtype=np.int64).astype(np.int32)
+        for lo in range(0, n):
+            for k in range(1, n - lo + 1):
+                M = np.kron(np.kron(np.eye(1 << (n - lo - k)), dense.hadamard_popc(k)), np.eye(1 << lo))
+                ref = x @ M.T * 2.0 ** (-k / 2.0)
+                assert _rel(orc.fwt_bits(x, lo, k, normalize=True), ref) < 1e-14, f"n={n} lo={lo} k={k}"
+                refi = ((xi.astype(np.int64) @ M.T.astype(np.int64)) % (1 << 32)).astype(np.uint32).view(np.int32)
+                assert np.array_equal(orc.fwt_bits(xi, lo, k, normalize=False), refi), f"int n={n} lo={lo} k={k}"
+    for n in (5, 12, 16):
+        x = rng.standard_normal((1, 1 << n))
+        assert _rel(orc.fwt_bits(x, 0, n, normalize=True), orc.fwt(x, normalize=True)) < 1e-15
+        cuts = sorted(set([0, n // 3, (2 * n) // 3, n]))
+        y = x
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            y = orc.fwt_bits(y, a, b - a, normalize=True)
+        assert _rel(y, orc.fwt(x, normalize=True)) < 1e-14, f"composition n={n}"
+        xi = rng.integers(-(2 ** 31), 2 ** 31, size=(1, 1 << n), dtype=np.int64).astype(np.int32)
+        twice = orc.fwt_bits(orc.fwt_bits(xi, 2, 3, normalize=False), 2, 3, normalize=False)
+        assert np.array_equal(twice, ((xi.astype(np.int64) << 3) % (1 << 32)).astype(np.uint32).view(np.int32))
+
+
 ORACLE_PINS = [
     pin_butterfly_vs_dense_float,
     pin_butterfly_vs_dense_int,
@@ -208,4 +236,5 @@ ORACLE_PINS = [
     pin_entries,
     pin_scale,
     pin_fp32_promotion,
+    pin_bit_range,
 ]

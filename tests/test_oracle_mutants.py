@@ -27,6 +27,12 @@ MUTANTS = [
     ("int entry transposed sign", "if (popc_parity((uint64_t)(k & i))) acc -= x[i];",
      "if (!popc_parity((uint64_t)(k & i))) acc -= x[i];", 0),
     ("scale skipped", "if (jb->scale != 1.0)", "if (jb->scale == 12345.0)", 0),
+    ("bit range starts one stage late", "for (int64_t h = (int64_t)1 << lo;",
+     "for (int64_t h = (int64_t)2 << lo;", 0),
+    ("bit range scale uses n", "oracle_scale(nbits, normalize), 0, nthreads, lo, nbits)",
+     "oracle_scale(n, normalize), 0, nthreads, lo, nbits)", 0),
+    ("u32 bit range drops the last stage", "for (int64_t h = (int64_t)1 << lo; h < ((int64_t)1 << (lo + nbits)); h *= 2) {\n    for (int64_t i = 0; i < N; i += 2 * h) {\n      for (int64_t j = i; j < i + h; ++j) {\n        uint32_t",
+     "for (int64_t h = (int64_t)1 << lo; 2 * h < ((int64_t)1 << (lo + nbits)); h *= 2) {\n    for (int64_t i = 0; i < N; i += 2 * h) {\n      for (int64_t j = i; j < i + h; ++j) {\n        uint32_t", 0),
 ]
 
 

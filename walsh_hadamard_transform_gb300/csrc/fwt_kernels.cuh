@@ -422,7 +422,8 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
 
 // ---- kernels --------------------------------------------------------------------
 // KIND: 0 = fp32, 1 = fp64 (fixed point), 2 = int32, 3 = fp64 plain IEEE
-// Two CTAs per SM for tiles up to 256 threads (at most 128 registers a thread).
+// At most 128 registers a thread, so that 512 threads (16 warps) fit an SM
+// whatever the tile size.
 template <class S, int KIND, class Mover>
 __device__ __forceinline__ void tile_body(const PassParams& p, unsigned char* smem_raw, Mover& mv) {
   if constexpr (KIND == 0) plain_tile<S, ArithF32, float>(p, smem_raw, mv);
@@ -432,7 +433,7 @@ __device__ __forceinline__ void tile_body(const PassParams& p, unsigned char* sm
 }
 
 template <class S, int KIND, bool COLS>
-__global__ void __launch_bounds__(S::NT, S::NT <= 256 ? 2 : 1) fwt_tile_kernel(const PassParams p) {
+__global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1)) fwt_tile_kernel(const PassParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   DirectMover<S, COLS> mv(p, smem_raw);
   tile_body<S, KIND>(p, smem_raw, mv);
@@ -440,7 +441,7 @@ __global__ void __launch_bounds__(S::NT, S::NT <= 256 ? 2 : 1) fwt_tile_kernel(c
 
 // Column pass with TMA-staged tiles.
 template <class S, int KIND>
-__global__ void __launch_bounds__(S::NT, S::NT <= 256 ? 2 : 1)
+__global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
     fwt_col_tma_kernel(const __grid_constant__ TmaPassParams tp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bar;
