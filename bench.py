@@ -54,6 +54,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(STEP_WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--bits", default="",
+                    help="LO,NBITS: time the transform over index bits [LO, LO+NBITS) only")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch of every part (small cases for profiling; 0 = as specified)")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -244,11 +246,24 @@ def run_ours(args):
         dev_out.append((torch.empty_like(dev_in[-1][0]), torch.empty_like(dev_in[-1][1])))
     torch.cuda.synchronize(device)
 
+    bits = tuple(int(v) for v in args.bits.split(",")) if args.bits else None
+
     def step():
         for w, (a, b), (c, d) in zip(parts, dev_in, dev_out):
-            fwt.transform(a, b, c, d, normalize=w.normalize)
+            fwt.transform(a, b, c, d, normalize=w.normalize, bits=bits)
 
-    names = [nm for w in parts for nm in pass_names(w, fwt)]
+    names, owners = [], []  # one entry per pass launched by a step, and its part
+    for pi, (w, (a, b), (c, d)) in enumerate(zip(parts, dev_in, dev_out)):
+        if bits is None:
+            part_names = pass_names(w, fwt)
+        else:  # count the passes of a bit-range transform from one traced call
+            tr = fwt.PassTrace([torch.cuda.Event(enable_timing=True) for _ in range(16)])
+            with tr:
+                fwt.transform(a, b, c, d, normalize=w.normalize, bits=bits)
+            part_names = [f"{w.dtype} bits [{bits[0]}, {bits[0] + bits[1]}) pass {i + 1} (n={w.n})"
+                          for i in range(tr.count // 2)]
+        names += part_names
+        owners += [pi] * len(part_names)
     launches_per_step = len(names)
     for _ in range(args.warmup):
         step()
@@ -291,14 +306,11 @@ def run_ours(args):
 
     # dominant kernel: largest share of device time
     kernels = []
-    li = 0
-    for w in parts:
-        for nm in pass_names(w, fwt):
-            mean_ms = statistics.mean(per_kernel[li])
-            algo = 2 * w.bytes_in  # every pass reads and writes the whole batch once
-            kernels.append({"kernel": nm, "mean_ms": mean_ms, "total_ms": sum(per_kernel[li]),
-                            "algo_bytes_per_launch": algo, "gbs": algo / (mean_ms * 1e-3) / 1e9})
-            li += 1
+    for li, (nm, pi) in enumerate(zip(names, owners)):
+        mean_ms = statistics.mean(per_kernel[li])
+        algo = 2 * parts[pi].bytes_in  # every pass reads and writes the whole batch once
+        kernels.append({"kernel": nm, "mean_ms": mean_ms, "total_ms": sum(per_kernel[li]),
+                        "algo_bytes_per_launch": algo, "gbs": algo / (mean_ms * 1e-3) / 1e9})
     top = max(kernels, key=lambda k: k["total_ms"])
     traffic = ncu_traffic(top["kernel"])
     roofline = {"bound": "hbm", "achieved": round(top["gbs"], 1), "peak": peak, "unit": "GB/s",
@@ -313,7 +325,8 @@ def run_ours(args):
         "dtype": "+".join(sorted({{"c64": "int64", "c32": "f32", "i32": "int32"}[w.dtype] for w in parts})),
         "data": "synthetic (seeded PCG64; Gaussian unit-L2 states / uniform ints, per the workload)",
         "config": {
-            "workload": args.workload if args.batch <= 0 else "%s (batch %d)" % (args.workload, args.batch),
+            "workload": (args.workload if args.batch <= 0 else "%s (batch %d)" % (args.workload, args.batch))
+                        + ("" if bits is None else " bits [%d, %d)" % (bits[0], bits[0] + bits[1])),
             "parts": [{"name": w.name, "n": w.n, "batch": w.batch, "dtype": w.dtype,
                        "normalize": w.normalize, "factors": fwt.plan_factors(w.n, w.dtype)}
                       for w in parts],

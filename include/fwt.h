@@ -88,6 +88,24 @@ int fwt_batched_c64(const double* re_in, const double* im_in, double* re_out, do
 int fwt_batched_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out,
                     int32_t* im_out, int n, int64_t batch, int normalize, fwt_stream_t stream);
 
+/*
+ * Transform on a range of index bits (qubits): y = (I (x) H_nbits (x) I_{2^lo}) x
+ * for each vector, i.e. the butterfly stages of index bits [lo, lo + nbits) only,
+ * scaled by 2^{-nbits/2} when normalising.  lo = 0, nbits = n is the whole
+ * transform; disjoint ranges compose, so a caller can apply the factors of a
+ * Kronecker split one at a time ("[QDP] [feature] Pr4 kronecker fwt",
+ * deliverables: (H_{n1} (x) I) and (I (x) H_{n2})).  0 <= lo, 0 <= nbits,
+ * lo + nbits <= n <= 30; other arguments, layout, in-place rules and errors as
+ * for fwt_batched_*.  Bits below 2^15 (2^14 for fp64) are handled in contiguous
+ * tiles, higher bits by strided column tiles, each pass one read and one write.
+ */
+int fwt_bits_c32(const float* re_in, const float* im_in, float* re_out, float* im_out, int n,
+                 int64_t batch, int lo, int nbits, int normalize, fwt_stream_t stream);
+int fwt_bits_c64(const double* re_in, const double* im_in, double* re_out, double* im_out, int n,
+                 int64_t batch, int lo, int nbits, int normalize, fwt_stream_t stream);
+int fwt_bits_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, int32_t* im_out,
+                 int n, int64_t batch, int lo, int nbits, int normalize, fwt_stream_t stream);
+
 /* Static text for a status code (never NULL). */
 const char* fwt_status_string(int status);
 
@@ -120,9 +138,10 @@ int fwt_plan_factors(int n, int dtype, int* bits, int max_factors);
 int fwt_set_plan(int n, int dtype, int nfactors, const int* bits);
 
 /*
- * Tuning: bytes of contiguous columns (64 or 128; also 32 for FWT_C64) that each
- * tile of a column pass reads from every row it touches.  Wider segments make
- * longer DRAM bursts; narrower ones shrink the tile so that two CTAs share an SM.
+ * Tuning: bytes of contiguous columns (16, 32, 64 or 128) that each tile of a
+ * column pass reads from every row it touches.  Wider segments make longer DRAM
+ * bursts; narrower ones shrink the tile so that more CTAs share an SM.  16-byte
+ * tiles are always staged by TMA copies.
  * Affects default plans and plans set afterwards for `dtype`.  Returns FWT_OK or
  * FWT_ERR_INVALID_ARG; fwt_get_column_bytes returns the current width (-1 for an
  * invalid dtype).

@@ -114,11 +114,11 @@ def test_plan_override_roundtrip(lib):
 
 def test_column_bytes_setting(lib):
     for dt in ("c32", "c64", "i32"):
-        assert fwt.column_bytes(dt) in (32, 64, 128)
+        assert fwt.column_bytes(dt) in (16, 32, 64, 128)
     with pytest.raises(fwt.FwtError):
         fwt.set_column_bytes("c32", 96)
     with pytest.raises(fwt.FwtError):
-        fwt.set_column_bytes("c32", 32)  # 32-byte column tiles exist for fp64 only
+        fwt.set_column_bytes("c32", 256)
     assert lib.fwt_get_column_bytes(5) == -1
 
 
@@ -145,3 +145,16 @@ def test_tma_setting(lib):
     with pytest.raises(fwt.FwtError):
         fwt.set_tma(3)
     fwt.set_tma(fwt.TMA_AUTO)
+
+
+@pytest.mark.parametrize("fn", ["fwt_bits_c32", "fwt_bits_c64", "fwt_bits_i32"])
+def test_bit_range_argument_errors_before_launch(lib, fn):
+    f = getattr(fwt, fn)
+    a, b, c, d = A, A + GiB, A + 2 * GiB, A + 3 * GiB
+    assert f(a, b, c, d, 8, 1, 0, 9, 0, None) == fwt.FWT_ERR_INVALID_ARG   # past n
+    assert f(a, b, c, d, 8, 1, -1, 2, 0, None) == fwt.FWT_ERR_INVALID_ARG  # lo < 0
+    assert f(a, b, c, d, 8, 1, 2, -1, 0, None) == fwt.FWT_ERR_INVALID_ARG  # nbits < 0
+    assert f(a, b, c, d, 31, 1, 0, 1, 0, None) == fwt.FWT_ERR_INVALID_ARG  # n > 30
+    assert f(a + 4, b, c, d, 8, 1, 0, 3, 0, None) == fwt.FWT_ERR_MISALIGNED
+    assert f(a, b, b, d, 8, 1, 0, 3, 0, None) == fwt.FWT_ERR_INVALID_ARG   # re_out over im_in
+    assert f(None, None, None, None, 8, 0, 0, 3, 0, None) == fwt.FWT_OK     # empty batch

@@ -77,7 +77,7 @@ def test_every_kronecker_split(dtype, n, tma):
     width = fwt.column_bytes(dtype)
     fwt.set_tma(tma)
     try:
-        for cb in ((32, 64, 128) if dtype == "c64" else (64, 128)):
+        for cb in ((16, 32, 64, 128) if tma == 2 else (32, 64, 128)):
             fwt.set_column_bytes(dtype, cb)
             plans = _valid_plans(n, dtype)
             assert plans, "no valid plan"

@@ -54,6 +54,10 @@ def library() -> ctypes.CDLL:
             f = getattr(lib, name)
             f.argtypes = [vp, vp, vp, vp, ci, i64, ci, vp]
             f.restype = ci
+        for name in ("fwt_bits_c32", "fwt_bits_c64", "fwt_bits_i32"):
+            f = getattr(lib, name)
+            f.argtypes = [vp, vp, vp, vp, ci, i64, ci, ci, ci, vp]
+            f.restype = ci
         lib.fwt_status_string.argtypes = [ci]
         lib.fwt_status_string.restype = ctypes.c_char_p
         lib.fwt_last_cuda_error.argtypes = []
@@ -100,6 +104,21 @@ def fwt_batched_c64(re_in, im_in, re_out, im_out, n, batch, normalize, stream) -
 
 def fwt_batched_i32(re_in, im_in, re_out, im_out, n, batch, normalize, stream) -> int:
     return library().fwt_batched_i32(re_in, im_in, re_out, im_out, n, batch, int(normalize), stream)
+
+
+def fwt_bits_c32(re_in, im_in, re_out, im_out, n, batch, lo, nbits, normalize, stream) -> int:
+    return library().fwt_bits_c32(re_in, im_in, re_out, im_out, n, batch, lo, nbits,
+                                  int(normalize), stream)
+
+
+def fwt_bits_c64(re_in, im_in, re_out, im_out, n, batch, lo, nbits, normalize, stream) -> int:
+    return library().fwt_bits_c64(re_in, im_in, re_out, im_out, n, batch, lo, nbits,
+                                  int(normalize), stream)
+
+
+def fwt_bits_i32(re_in, im_in, re_out, im_out, n, batch, lo, nbits, normalize, stream) -> int:
+    return library().fwt_bits_i32(re_in, im_in, re_out, im_out, n, batch, lo, nbits,
+                                  int(normalize), stream)
 
 
 def status_string(status: int) -> str:
@@ -209,6 +228,7 @@ class PassTrace:
 # ---- tensor-level wrapper ---------------------------------------------------------
 
 _ENTRY = {"c32": fwt_batched_c32, "c64": fwt_batched_c64, "i32": fwt_batched_i32}
+_BITS_ENTRY = {"c32": fwt_bits_c32, "c64": fwt_bits_c64, "i32": fwt_bits_i32}
 
 
 def _dtype_key(t) -> str:
@@ -220,13 +240,16 @@ def _dtype_key(t) -> str:
     return key
 
 
-def transform(re, im=None, out_re=None, out_im=None, normalize: bool = True, stream=None):
+def transform(re, im=None, out_re=None, out_im=None, normalize: bool = True, stream=None,
+              bits=None):
     """Transform the rows of ``re`` / ``im`` (CUDA tensors of shape (batch, 2^n)).
 
     Outputs are new tensors unless ``out_re`` / ``out_im`` are given (they may be
     the inputs themselves, for an in-place transform).  ``im`` may be None only
     for int32 (real-only input).  Runs on ``stream`` (default: the current
-    PyTorch stream); the call does not synchronise.  Returns (out_re, out_im).
+    PyTorch stream); the call does not synchronise.  ``bits=(lo, nbits)``
+    transforms index bits [lo, lo + nbits) only (I (x) H_nbits (x) I).  Returns
+    (out_re, out_im).
     """
     import torch
 
@@ -253,12 +276,16 @@ def transform(re, im=None, out_re=None, out_im=None, normalize: bool = True, str
     if stream is None:
         stream = torch.cuda.current_stream(re.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    ptrs = (re.data_ptr(), im.data_ptr() if im is not None else None, out_re.data_ptr(),
+            out_im.data_ptr() if out_im is not None else None)
     with torch.cuda.device(re.device):
-        st = _ENTRY[key](re.data_ptr(), im.data_ptr() if im is not None else None,
-                         out_re.data_ptr(), out_im.data_ptr() if out_im is not None else None,
-                         n, batch, normalize, handle)
+        if bits is None:
+            st = _ENTRY[key](*ptrs, n, batch, normalize, handle)
+        else:
+            st = _BITS_ENTRY[key](*ptrs, n, batch, int(bits[0]), int(bits[1]), normalize, handle)
     if st != FWT_OK:
-        raise FwtError(st, f"fwt_batched_{key}(n={n}, batch={batch})")
+        what = f"fwt_batched_{key}" if bits is None else f"fwt_bits_{key}(bits={tuple(bits)})"
+        raise FwtError(st, f"{what}(n={n}, batch={batch})")
     return out_re, out_im
 
 

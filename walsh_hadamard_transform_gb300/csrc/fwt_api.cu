@@ -26,9 +26,12 @@ thread_local int g_trace_count = 0;
 const std::vector<KernelEntry>& table() {
   static const std::vector<KernelEntry> t = [] {
     std::vector<KernelEntry> v;
-    register_c32(v);
-    register_c64(v);
-    register_i32(v);
+    register_rows_c32(v);
+    register_rows_c64(v);
+    register_rows_i32(v);
+    register_cols_c32(v);
+    register_cols_c64(v);
+    register_cols_i32(v);
     return v;
   }();
   return t;
@@ -57,7 +60,10 @@ struct Plan {
 
 // TMA staging pays for column tiles with many rows (long strided walks); short
 // tiles are faster with plain vector loads (measured on GB300).
-int col_tma(const Plan& p, int K) { return p.tma == 2 || (p.tma == 1 && K >= 10) ? 1 : 0; }
+// 16-byte segments exist only as TMA tiles.
+int col_tma(const Plan& p, int K) {
+  return p.tma == 2 || p.col_bytes == 16 || (p.tma == 1 && K >= 10) ? 1 : 0;
+}
 
 std::mutex g_plan_mu;
 Plan g_override[3][31];  // nf == 0: no override
@@ -67,9 +73,11 @@ int g_use_tma = 1;                    // TMA-staged column passes: 0 never, 1 au
 int max_row_bits(int dtype) { return dtype == FWT_C64 ? 14 : 15; }
 // column factors available for a segment width: tiles of 2^10 .. 2^15 (2^14 fp64) elements
 int min_col_bits(int dtype, int cb) {
-  return (dtype == FWT_C64 ? 6 : 5) + (cb == 64 ? 1 : cb == 32 ? 2 : 0);
+  return (dtype == FWT_C64 ? 6 : 5) + (cb == 64 ? 1 : cb == 32 ? 2 : cb == 16 ? 3 : 0);
 }
-int max_col_bits(int, int cb) { return cb == 128 ? 10 : cb == 64 ? 11 : 12; }
+int max_col_bits(int dtype, int cb) {
+  return min_col_bits(dtype, cb) + (dtype == FWT_C64 ? 4 : 5);  // tiles up to 2^14 / 2^15
+}
 
 bool plan_valid(int n, int dtype, const Plan& p) {
   if (p.nf < 1 || p.nf > 3) return false;
@@ -188,18 +196,94 @@ bool overlaps(const void* a, const void* b, size_t bytes) {
   return x < y + bytes && y < x + bytes;
 }
 
-int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out, int n,
-        int64_t batch, int normalize, cudaStream_t stream) {
-  if (n < 0 || n > 30 || batch < 0) return FWT_ERR_INVALID_ARG;
-  if (dtype == FWT_I32 && normalize) return FWT_ERR_UNSUPPORTED;
-  if (batch == 0) return FWT_OK;
+// One launch of a pass kernel over the whole batch (or one chunk of it).
+struct PassSpec {
+  const KernelEntry* e;
+  int L;        // column passes: log2 of the row stride
+  int bits_lo;  // run-time bit-range row passes: first transformed tile bit
+  int bits_k;   //   ... and how many
+};
+
+// The column pass over bits [L, L + K): the plan's segment width when a tile
+// shape exists for it, else another width, else (K <= 4) a wide-segment tile.
+const KernelEntry* column_kernel(int dtype, int K, int L, const Plan& plan) {
+  const int widths[5] = {plan.col_bytes, 128, 64, 32, 16};
+  for (int cb : widths) {
+    for (int tma : {col_tma(plan, K), 1 - col_tma(plan, K)}) {
+      const KernelEntry* e = find_kernel(dtype, KIND_COL, K, cb, tma);
+      if (e && L >= e->TS) return e;
+    }
+  }
+  const int esz = elem_size(dtype);
+  if (K <= 5) {  // short factors: wide segments of 2^(10-K) elements
+    const KernelEntry* e = find_kernel(dtype, KIND_COL, K, (1 << (10 - K)) * esz, 0);
+    if (e && L >= e->TS) return e;
+  }
+  return nullptr;
+}
+
+// Passes of the whole transform for a Kronecker plan (factor 0 = row pass).
+bool full_passes(int n, int dtype, const Plan& plan, std::vector<PassSpec>& out) {
+  int L = 0;
+  for (int f = 0; f < plan.nf; ++f) {
+    const int K = plan.bits[f];
+    PassSpec ps{nullptr, L, 0, 0};
+    if (f == 0) ps.e = find_kernel(dtype, K <= 2 ? KIND_SMALL : KIND_ROW, K);
+    else ps.e = find_kernel(dtype, KIND_COL, K, plan.col_bytes, col_tma(plan, K));
+    if (!ps.e) return false;
+    out.push_back(ps);
+    L += K;
+  }
+  return L == n;
+}
+
+// Passes of the transform over index bits [lo, lo + k) only: bits below the
+// largest row tile go to one run-time bit-range row pass, the rest to column
+// passes of at most 10 bits each.
+bool range_passes(int n, int dtype, int lo, int k, const Plan& plan, std::vector<PassSpec>& out) {
+  const int rmax = max_row_bits(dtype);
+  const int hi = lo + k;
+  if (lo == 0 && k == n) return full_passes(n, dtype, plan, out);
+  if (lo == 0 && k >= 3 && k <= rmax) {  // the low k bits: a plain row pass
+    const KernelEntry* e = find_kernel(dtype, KIND_ROW, k);
+    if (!e) return false;
+    out.push_back(PassSpec{e, 0, 0, 0});
+    return true;
+  }
+  if (hi <= rmax || k == 0) {
+    const int tb = std::max(hi, 10);
+    const KernelEntry* e = find_kernel(dtype, KIND_ROWBITS, std::min(tb, rmax));
+    if (!e) return false;
+    out.push_back(PassSpec{e, 0, lo, k});
+    return true;
+  }
+  int L = lo;
+  if (lo < rmax) {  // bits [lo, rmax) in row tiles of 2^rmax elements
+    const KernelEntry* e = find_kernel(dtype, KIND_ROWBITS, rmax);
+    if (!e) return false;
+    out.push_back(PassSpec{e, 0, lo, rmax - lo});
+    L = rmax;
+  }
+  const int rest = hi - L;
+  const int nf = (rest + 9) / 10;
+  for (int f = 0; f < nf; ++f) {
+    const int K = rest / nf + (f < rest % nf ? 1 : 0);
+    const KernelEntry* e = column_kernel(dtype, K, L, plan);
+    if (!e) return false;
+    out.push_back(PassSpec{e, L, 0, 0});
+    L += K;
+  }
+  return true;
+}
+
+int check_arrays(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out,
+                 int n, int64_t batch, bool& has_im) {
   const int esz = elem_size(dtype);
   if (batch > (INT64_MAX >> n) / esz) return FWT_ERR_INVALID_ARG;
-  const long long comp_elems = (long long)batch << n;
-  const size_t bytes = (size_t)comp_elems * (size_t)esz;
+  const size_t bytes = (size_t)(((long long)batch << n) * esz);
   // pointers: real part required; imaginary part both-or-neither (NULL only for int32)
   if (!re_in || !re_out) return FWT_ERR_INVALID_ARG;
-  const bool has_im = im_in || im_out;
+  has_im = im_in || im_out;
   if (has_im && (!im_in || !im_out)) return FWT_ERR_INVALID_ARG;
   if (!has_im && dtype != FWT_I32) return FWT_ERR_INVALID_ARG;
   const void* ptrs[4] = {re_in, im_in, re_out, im_out};
@@ -213,8 +297,23 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
         overlaps(im_out, re_in, bytes))
       return FWT_ERR_INVALID_ARG;
   }
-  Plan plan = get_plan(n, dtype);
-  if (!plan_valid(n, dtype, plan)) return FWT_ERR_UNSUPPORTED;
+  return FWT_OK;
+}
+
+// Runs the transform over bits [lo, lo + k) of each vector (the whole transform
+// when lo = 0, k = n), scaled by 2^{-k/2} when normalising.
+int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out, int n,
+        int64_t batch, int lo, int k, int normalize, cudaStream_t stream) {
+  if (n < 0 || n > 30 || batch < 0 || lo < 0 || k < 0 || lo + k > n) return FWT_ERR_INVALID_ARG;
+  if (dtype == FWT_I32 && normalize) return FWT_ERR_UNSUPPORTED;
+  if (batch == 0) return FWT_OK;
+  bool has_im = false;
+  int st = check_arrays(dtype, re_in, im_in, re_out, im_out, n, batch, has_im);
+  if (st != FWT_OK) return st;
+  const int esz = elem_size(dtype);
+  const bool whole = lo == 0 && k == n;
+  Plan plan = whole ? get_plan(n, dtype) : default_plan(n, dtype);
+  if (whole && !plan_valid(n, dtype, plan)) return FWT_ERR_UNSUPPORTED;
 
   cudaError_t err = ensure_device();
   if (err != cudaSuccess) {
@@ -222,13 +321,15 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
     return FWT_ERR_CUDA;
   }
   if (plan.tma && !tensor_map_encoder()) plan.tma = 0;  // driver without the TMA encoder
+  std::vector<PassSpec> passes;
+  if (!range_passes(n, dtype, lo, k, plan, passes)) return FWT_ERR_UNSUPPORTED;
 
   PassParams p{};
-  const double s = n % 2 == 0 ? std::ldexp(1.0, -n / 2) : std::ldexp(1.0, -(n - 1) / 2) / std::sqrt(2.0);
+  const double s = k % 2 == 0 ? std::ldexp(1.0, -k / 2) : std::ldexp(1.0, -(k - 1) / 2) / std::sqrt(2.0);
   p.scale_f64 = s;
   p.scale_f32 = (float)s;
-  p.scale_exp = -(n / 2);
-  p.scale_half = n % 2;
+  p.scale_exp = -(k / 2);
+  p.scale_half = k % 2;
   p.rsqrt2_q64 = rsqrt2_q64();
 
   // L2 chunking (opt-in): a multi-pass transform runs all its passes on one
@@ -244,7 +345,8 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
   long long vpc = batch;  // vectors per chunk
   int parts_per_launch = ncomp_all;
   bool chunked = false;
-  if (plan.nf >= 2 && budget > 0) {
+  const int npass = (int)passes.size();
+  if (npass >= 2 && budget > 0) {
     if ((long long)ncomp_all * vec_bytes <= budget) {
       vpc = std::max(1ll, budget / (ncomp_all * vec_bytes));
     } else if (vec_bytes <= budget) {
@@ -260,33 +362,36 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
       const long long nv = std::min(vpc, batch - v0);
       const long long off = (v0 << n) * esz;  // byte offset of the chunk
       const long long elems = nv << n;
-      int L = 0;
-      for (int f = 0; f < plan.nf; ++f) {
-        const int K = plan.bits[f];
-        const KernelEntry* e;
+      for (int f = 0; f < npass; ++f) {
+        const PassSpec& ps = passes[f];
+        const KernelEntry* e = ps.e;
         long long tiles;
-        if (f == 0 && K <= 2) {
-          e = find_kernel(dtype, KIND_SMALL, K);
-          tiles = ((elems >> K) + 255) / 256;
-        } else if (f == 0) {
-          e = find_kernel(dtype, KIND_ROW, K);
-          tiles = (elems + (1ll << e->TB) - 1) >> e->TB;
-        } else {
-          e = find_kernel(dtype, KIND_COL, K, plan.col_bytes, col_tma(plan, K));
-          tiles = elems >> e->TB;
-        }
+        if (e->kind == KIND_SMALL) tiles = ((elems >> e->K) + 255) / 256;
+        else if (e->kind == KIND_COL) tiles = elems >> e->TB;
+        else tiles = (elems + (1ll << e->TB) - 1) >> e->TB;
         if (tiles > INT_MAX) return FWT_ERR_UNSUPPORTED;
         p.comp_elems = elems;
+        bool in_place = true;
         for (int c = 0; c < 2; ++c) {
           const int part = part0 + (c < parts_per_launch ? c : 0);
           const char* src = (const char*)(f == 0 ? ins[part] : outs[part]);
           p.in[c] = src ? src + off : nullptr;
           p.out[c] = outs[part] ? (char*)outs[part] + off : nullptr;
+          in_place &= p.in[c] == p.out[c];
         }
-        p.stride_log = L;
-        const bool last = f == plan.nf - 1;
+        if (e->tma && !in_place) {  // TMA column tiles run in place; copy-in passes load directly
+          const KernelEntry* d = find_kernel(dtype, KIND_COL, e->K, e->col_bytes, 0);
+          if (!d) d = column_kernel(dtype, e->K, ps.L, Plan{0, {0, 0, 0}, 128, 0});
+          if (!d) return FWT_ERR_UNSUPPORTED;
+          e = d;
+          tiles = elems >> e->TB;
+        }
+        p.stride_log = ps.L;
+        p.bits_lo = ps.bits_lo;
+        p.bits_k = ps.bits_k;
+        const bool last = f == npass - 1;
         p.do_scale = (normalize && last) ? 1 : 0;
-        p.ld_policy = 1;                          // read once
+        p.ld_policy = 1;                             // read once
         p.st_policy = last ? 1 : (chunked ? 2 : 0);  // keep intermediates for the next pass
         const bool traced = g_trace_count + 2 <= g_trace_capacity;
         if (traced) {
@@ -305,7 +410,6 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
           g_last_cuda_error = (int)err;
           return FWT_ERR_CUDA;
         }
-        L += K;
       }
     }
   }
@@ -332,17 +436,41 @@ extern "C" {
 
 int fwt_batched_c32(const float* re_in, const float* im_in, float* re_out, float* im_out, int n,
                     int64_t batch, int normalize, fwt_stream_t stream) {
-  return fwt::run(FWT_C32, re_in, im_in, re_out, im_out, n, batch, normalize, (cudaStream_t)stream);
+  if (n < 0 || n > 30) return FWT_ERR_INVALID_ARG;
+  return fwt::run(FWT_C32, re_in, im_in, re_out, im_out, n, batch, 0, n, normalize,
+                  (cudaStream_t)stream);
 }
 
 int fwt_batched_c64(const double* re_in, const double* im_in, double* re_out, double* im_out,
                     int n, int64_t batch, int normalize, fwt_stream_t stream) {
-  return fwt::run(FWT_C64, re_in, im_in, re_out, im_out, n, batch, normalize, (cudaStream_t)stream);
+  if (n < 0 || n > 30) return FWT_ERR_INVALID_ARG;
+  return fwt::run(FWT_C64, re_in, im_in, re_out, im_out, n, batch, 0, n, normalize,
+                  (cudaStream_t)stream);
 }
 
 int fwt_batched_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, int32_t* im_out,
                     int n, int64_t batch, int normalize, fwt_stream_t stream) {
-  return fwt::run(FWT_I32, re_in, im_in, re_out, im_out, n, batch, normalize, (cudaStream_t)stream);
+  if (n < 0 || n > 30) return FWT_ERR_INVALID_ARG;
+  return fwt::run(FWT_I32, re_in, im_in, re_out, im_out, n, batch, 0, n, normalize,
+                  (cudaStream_t)stream);
+}
+
+int fwt_bits_c32(const float* re_in, const float* im_in, float* re_out, float* im_out, int n,
+                 int64_t batch, int lo, int nbits, int normalize, fwt_stream_t stream) {
+  return fwt::run(FWT_C32, re_in, im_in, re_out, im_out, n, batch, lo, nbits, normalize,
+                  (cudaStream_t)stream);
+}
+
+int fwt_bits_c64(const double* re_in, const double* im_in, double* re_out, double* im_out, int n,
+                 int64_t batch, int lo, int nbits, int normalize, fwt_stream_t stream) {
+  return fwt::run(FWT_C64, re_in, im_in, re_out, im_out, n, batch, lo, nbits, normalize,
+                  (cudaStream_t)stream);
+}
+
+int fwt_bits_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, int32_t* im_out,
+                 int n, int64_t batch, int lo, int nbits, int normalize, fwt_stream_t stream) {
+  return fwt::run(FWT_I32, re_in, im_in, re_out, im_out, n, batch, lo, nbits, normalize,
+                  (cudaStream_t)stream);
 }
 
 const char* fwt_status_string(int status) {
@@ -389,8 +517,7 @@ int fwt_set_plan(int n, int dtype, int nfactors, const int* bits) {
 }
 
 int fwt_set_column_bytes(int dtype, int bytes) {
-  if (dtype < 0 || dtype > 2 || (bytes != 32 && bytes != 64 && bytes != 128) ||
-      (bytes == 32 && dtype != FWT_C64))
+  if (dtype < 0 || dtype > 2 || (bytes != 16 && bytes != 32 && bytes != 64 && bytes != 128))
     return FWT_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
   fwt::g_col_bytes[dtype] = bytes;

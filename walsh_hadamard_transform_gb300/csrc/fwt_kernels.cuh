@@ -50,6 +50,7 @@ struct PassParams {
   unsigned long long rsqrt2_q64;  // floor(2^64 / sqrt(2))
   int ld_policy;         // L2 eviction priority of the loads: 0 normal, 1 first, 2 last
   int st_policy;         // ... and of the stores
+  int bits_lo, bits_k;   // run-time bit-range tiles: transformed tile bits [lo, lo + k)
 };
 
 // ---- arithmetic policies ----------------------------------------------------------
@@ -105,7 +106,7 @@ __device__ __forceinline__ void stg16(void* p, const typename Vec16<U>::type& va
 }
 
 // Tile-local index -> element offset within the array.
-template <class S, bool COLS>
+template <class S, bool COLS, bool RAGGED = (!COLS && S::TB > S::TK)>
 struct TileMap {
   long long base;
   int L;
@@ -119,7 +120,7 @@ struct TileMap {
     }
   }
   __device__ __forceinline__ bool in_range(uint32_t u) const {
-    if constexpr (!COLS && S::TB > S::TK) return (long long)u < valid;  // ragged last tile
+    if constexpr (RAGGED) return (long long)u < valid;  // ragged last tile
     else return true;
   }
   __device__ static TileMap make(const PassParams& p, long long tile) {
@@ -139,9 +140,8 @@ struct TileMap {
   }
 };
 
-template <class S, bool COLS, typename T, typename U>
-__device__ __forceinline__ void load_tile(const T* in, const TileMap<S, COLS>& m, U (&x)[S::NE],
-                                          int policy) {
+template <class S, class Map, typename T, typename U>
+__device__ __forceinline__ void load_tile(const T* in, const Map& m, U (&x)[S::NE], int policy) {
   using V = typename Vec16<U>::type;
   const uint32_t t = threadIdx.x;
   const unsigned long long pol = l2_policy(policy);
@@ -157,9 +157,8 @@ __device__ __forceinline__ void load_tile(const T* in, const TileMap<S, COLS>& m
   }
 }
 
-template <class S, bool COLS, typename T, typename U>
-__device__ __forceinline__ void store_tile(T* out, const TileMap<S, COLS>& m, const U (&x)[S::NE],
-                                           int policy) {
+template <class S, class Map, typename T, typename U>
+__device__ __forceinline__ void store_tile(T* out, const Map& m, const U (&x)[S::NE], int policy) {
   using V = typename Vec16<U>::type;
   const uint32_t t = threadIdx.x;
   const unsigned long long pol = l2_policy(policy);
@@ -176,25 +175,26 @@ __device__ __forceinline__ void store_tile(T* out, const TileMap<S, COLS>& m, co
 
 // ---- tile movers: HBM <-> registers ----------------------------------------------
 // Direct: 16-byte vector loads into layout L1, stores from layout L3.
-template <class S, bool COLS>
+template <class S, bool COLS, bool RAGGED = (!COLS && S::TB > S::TK)>
 struct DirectMover {
-  TileMap<S, COLS> m;
+  using Map = TileMap<S, COLS, RAGGED>;
+  Map m;
   const void* in;
   void* out;
   __device__ DirectMover(const PassParams& p, unsigned char*) {
     const bool im = blockIdx.y != 0;
     in = im ? p.in[1] : p.in[0];
     out = im ? p.out[1] : p.out[0];
-    m = TileMap<S, COLS>::make(p, (long long)blockIdx.x);
+    m = Map::make(p, (long long)blockIdx.x);
   }
   template <typename U>
   __device__ __forceinline__ bool load(U (&x)[S::NE], int policy) {
-    load_tile<S, COLS>(static_cast<const U*>(in), m, x, policy);
+    load_tile<S>(static_cast<const U*>(in), m, x, policy);
     return true;
   }
   template <typename U>
   __device__ __forceinline__ void store(const U (&x)[S::NE], int policy) {
-    store_tile<S, COLS>(static_cast<U*>(out), m, x, policy);
+    store_tile<S>(static_cast<U*>(out), m, x, policy);
   }
 };
 
@@ -263,12 +263,34 @@ struct TmaMover {
   }
 };
 
+// Which tile bits a pass transforms: fixed by the shape, or given at run time.
+template <class S>
+struct StaticBits {
+  static constexpr uint32_t r1 = S::RM1, r2 = S::RM2, r3 = S::RM3;
+  static constexpr int tk = S::TK;
+  __device__ explicit StaticBits(const PassParams&) {}
+};
+template <class S>
+struct RuntimeBits {
+  uint32_t r1, r2, r3;
+  int tk;
+  __device__ explicit RuntimeBits(const PassParams& p) {
+    uint32_t rm[3];
+    S::round_masks(p.bits_lo, p.bits_k, rm);
+    r1 = rm[0];
+    r2 = rm[1];
+    r3 = rm[2];
+    tk = p.bits_k;
+  }
+};
+
 // ---- fp32 / int32 / plain fp64 tile ---------------------------------------------
-template <class S, class A, typename T, class Mover>
-__device__ __forceinline__ void plain_tile(const PassParams& p, unsigned char* smem_raw, Mover& mv) {
+template <class S, class A, typename T, class Mover, class Bits>
+__device__ __forceinline__ void plain_tile(const PassParams& p, unsigned char* smem_raw, Mover& mv,
+                                           const Bits& bits) {
   T x[S::NE];
   if (!mv.load(x, p.ld_policy)) return;
-  tile_rounds<S, A>(x, reinterpret_cast<T*>(smem_raw));
+  tile_rounds<S, A>(x, reinterpret_cast<T*>(smem_raw), bits.r1, bits.r2, bits.r3);
   if (p.do_scale) {
     if constexpr (sizeof(T) == 4 && !std::is_integral<T>::value) {
 #pragma unroll
@@ -291,8 +313,9 @@ __device__ __forceinline__ uint32_t abs_hi(long long bits) {
 
 // q = round(v * 2^(F + 1023 - emax)), ties away from zero, for |v| < 2^(emax - 1022):
 // |q| <= 2^(F+1).  Integer bit arithmetic only.
-template <int F>
-__device__ __forceinline__ long long to_fixed(long long bits, int emax) {
+// RIGHT: F <= 52, so every element shifts right (the common case, branch-free).
+template <bool RIGHT>
+__device__ __forceinline__ long long to_fixed(long long bits, int emax, int F) {
   const unsigned long long b = (unsigned long long)bits;
   const int e = (int)((uint32_t)(b >> 32) >> 20) & 0x7ff;
   const unsigned long long m =
@@ -300,7 +323,7 @@ __device__ __forceinline__ long long to_fixed(long long bits, int emax) {
   // v = m * 2^(max(e,1) - 1075), so q = m * 2^(max(e,1) - emax + F - 52)
   const int sh = max(e, 1) - emax + F - 52;
   unsigned long long mag;
-  if constexpr (F <= 52) {  // sh <= F - 52 <= 0: always a rounding right shift
+  if constexpr (RIGHT) {  // sh <= F - 52 <= 0: always a rounding right shift
     const int rs = min(-sh, 63);
     mag = (((m << 1) >> rs) + 1ull) >> 1;
   } else if (sh >= 0) {
@@ -368,8 +391,9 @@ __device__ __forceinline__ long long from_fixed_cvt(long long q, long long e0_fi
   return q == 0 ? 0ll : b + e0_field;
 }
 
-template <class S, class Mover>
-__device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* smem_raw, Mover& mv) {
+template <class S, class Mover, class Bits>
+__device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* smem_raw, Mover& mv,
+                                           const Bits& bits) {
   __shared__ uint32_t red[32];
   long long x[S::NE];
   if (!mv.load(x, p.ld_policy)) return;
@@ -387,7 +411,8 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
     double xd[S::NE];
 #pragma unroll
     for (int r = 0; r < S::NE; ++r) xd[r] = __longlong_as_double(x[r]);
-    tile_rounds<S, ArithF64>(xd, reinterpret_cast<double*>(smem_raw));
+    tile_rounds<S, ArithF64>(xd, reinterpret_cast<double*>(smem_raw), bits.r1, bits.r2,
+                             bits.r3);
     if (p.do_scale) {
 #pragma unroll
       for (int r = 0; r < S::NE; ++r) xd[r] = xd[r] * p.scale_f64;
@@ -396,10 +421,16 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
     return;
   }
   const int emax = max((int)(key >> 20), 1);  // zeros and subnormals scale as exponent 1
-  constexpr int F = 61 - S::TK;  // headroom: |q| <= 2^(F+1) grows by 2^TK
+  const int F = 61 - bits.tk;  // headroom: |q| <= 2^(F+1) grows by 2^tk
+  if (F <= 52) {  // (uniform) every element shifts right: the common case
 #pragma unroll
-  for (int r = 0; r < S::NE; ++r) x[r] = to_fixed<F>(x[r], emax);
-  tile_rounds<S, ArithI64>(x, reinterpret_cast<long long*>(smem_raw));
+    for (int r = 0; r < S::NE; ++r) x[r] = to_fixed<true>(x[r], emax, F);
+  } else {
+#pragma unroll
+    for (int r = 0; r < S::NE; ++r) x[r] = to_fixed<false>(x[r], emax, F);
+  }
+  tile_rounds<S, ArithI64>(x, reinterpret_cast<long long*>(smem_raw), bits.r1, bits.r2,
+                           bits.r3);
   const int e0 = emax - 1023 - F + (p.do_scale ? p.scale_exp : 0);
   const int half = p.do_scale ? p.scale_half : 0;
   // every nonzero |q| lies in [1, 2^63): results are normal numbers iff
@@ -424,19 +455,31 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
 // KIND: 0 = fp32, 1 = fp64 (fixed point), 2 = int32, 3 = fp64 plain IEEE
 // At most 128 registers a thread, so that 512 threads (16 warps) fit an SM
 // whatever the tile size.
-template <class S, int KIND, class Mover>
-__device__ __forceinline__ void tile_body(const PassParams& p, unsigned char* smem_raw, Mover& mv) {
-  if constexpr (KIND == 0) plain_tile<S, ArithF32, float>(p, smem_raw, mv);
-  else if constexpr (KIND == 1) fixed_tile<S>(p, smem_raw, mv);
-  else if constexpr (KIND == 2) plain_tile<S, ArithU32, uint32_t>(p, smem_raw, mv);
-  else plain_tile<S, ArithF64, double>(p, smem_raw, mv);
+template <class S, int KIND, class Mover, class Bits>
+__device__ __forceinline__ void tile_body(const PassParams& p, unsigned char* smem_raw, Mover& mv,
+                                          const Bits& bits) {
+  if constexpr (KIND == 0) plain_tile<S, ArithF32, float>(p, smem_raw, mv, bits);
+  else if constexpr (KIND == 1) fixed_tile<S>(p, smem_raw, mv, bits);
+  else if constexpr (KIND == 2) plain_tile<S, ArithU32, uint32_t>(p, smem_raw, mv, bits);
+  else plain_tile<S, ArithF64, double>(p, smem_raw, mv, bits);
 }
 
 template <class S, int KIND, bool COLS>
 __global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1)) fwt_tile_kernel(const PassParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   DirectMover<S, COLS> mv(p, smem_raw);
-  tile_body<S, KIND>(p, smem_raw, mv);
+  tile_body<S, KIND>(p, smem_raw, mv, StaticBits<S>(p));
+}
+
+// Contiguous tiles of 2^TB elements whose transformed bits [bits_lo, bits_lo +
+// bits_k) are chosen at run time: a transform on a sub-range of the index bits
+// that lies within the low TB bits (several vectors per tile when 2^n < 2^TB).
+template <class S, int KIND>
+__global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
+    fwt_rowbits_kernel(const PassParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  DirectMover<S, false, true> mv(p, smem_raw);
+  tile_body<S, KIND>(p, smem_raw, mv, RuntimeBits<S>(p));
 }
 
 // Column pass with TMA-staged tiles.
@@ -446,7 +489,7 @@ __global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bar;
   TmaMover<S> mv(tp, smem_raw, &bar);
-  tile_body<S, KIND>(tp.p, smem_raw, mv);
+  tile_body<S, KIND>(tp.p, smem_raw, mv, StaticBits<S>(tp.p));
 }
 
 // Vectors of 2^NL <= 4 elements: one thread per vector, plain arithmetic.
@@ -460,7 +503,7 @@ __global__ void __launch_bounds__(256) fwt_small_kernel(const PassParams p) {
   T x[1 << NL];
 #pragma unroll
   for (int i = 0; i < (1 << NL); ++i) x[i] = in[(row << NL) + i];
-  butterflies<(1u << NL) - 1u, A>(x);
+  butterflies<A>(x, (1u << NL) - 1u);
   if (p.do_scale) {
 #pragma unroll
     for (int i = 0; i < (1 << NL); ++i) {

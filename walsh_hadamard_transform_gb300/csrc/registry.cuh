@@ -12,7 +12,7 @@
 
 namespace fwt {
 
-enum PassKind { KIND_SMALL = 0, KIND_ROW = 1, KIND_COL = 2 };
+enum PassKind { KIND_SMALL = 0, KIND_ROW = 1, KIND_COL = 2, KIND_ROWBITS = 3 };
 
 struct KernelEntry {
   int dtype;  // FWT_C32 / FWT_C64 / FWT_I32
@@ -67,7 +67,9 @@ inline int smem_wavefronts(const uint32_t* byte_addr, int bytes) {
   return total;
 }
 
-template <class S, bool COLS>
+// DIRECT: the tile is loaded and stored with 16-byte vector accesses (rather than
+// TMA copies), so its global accesses must fill whole sectors too.
+template <class S, bool COLS, bool DIRECT = true>
 int check_shape(const char* name) {
   int fails = 0;
   const uint32_t n = 1u << S::TB;
@@ -155,7 +157,7 @@ int check_shape(const char* name) {
   // 5. global accesses: every warp-wide 16-byte load (L1) and store (L3) fills
   //    whole 32-byte sectors (row tiles: 512 contiguous bytes)
   const int L = COLS ? S::TS + 3 : 0;  // any row stride >= the column width
-  for (int layout = 1; layout <= 3; layout += 2)
+  for (int layout = 1; DIRECT && layout <= 3; layout += 2)
     for (uint32_t w = 0; w < (uint32_t)S::NT / 32; ++w)
       for (int j = 0; j < S::NV; ++j) {
         std::vector<long long> sectors;
@@ -257,7 +259,7 @@ KernelEntry row_entry() {
 // (CB = 32, 64 or 128: two, four or eight 16-byte vectors).
 template <int DT, int KIND, int LV, int K, int CB, bool TMA>
 KernelEntry col_entry() {
-  constexpr int CWL = LV + (CB == 128 ? 3 : CB == 64 ? 2 : 1);
+  constexpr int CWL = ilog2c(CB) - ilog2c(16 >> LV);  // log2 columns of CB bytes
   constexpr int TB = K + CWL;
   constexpr int EL = choose_el(TB, LV);
   using S = Shape<TB, CWL, K, LV, TB - EL>;
@@ -269,7 +271,7 @@ KernelEntry col_entry() {
   if constexpr (TMA) {
     e.launch = &launch_col_tma<S, KIND>;
     e.setup = &setup_col_tma<S, KIND>;
-    e.selfcheck = &selfcheck_none;  // same shape as the direct kernel, checked there
+    e.selfcheck = [] { return check_shape<S, true, false>("col tma"); };
     e.fn = (const void*)&fwt_col_tma_kernel<S, KIND>;
   } else {
     e.launch = &launch_tile<S, KIND, true>;
@@ -277,6 +279,57 @@ KernelEntry col_entry() {
     e.selfcheck = [] { return check_shape<S, true>("col"); };
     e.fn = (const void*)&fwt_tile_kernel<S, KIND, true>;
   }
+  return e;
+}
+
+template <class S, int KIND>
+cudaError_t launch_rowbits(const PassParams& p, long long tiles, int ncomp, cudaStream_t st) {
+  const size_t smem = (size_t)(1u << S::TB) * (KIND == 1 || KIND == 3 ? 8 : 4);
+  fwt_rowbits_kernel<S, KIND><<<dim3((unsigned)tiles, (unsigned)ncomp), S::NT, smem, st>>>(p);
+  return cudaGetLastError();
+}
+template <class S, int KIND>
+cudaError_t setup_rowbits() {
+  const size_t smem = (size_t)(1u << S::TB) * (KIND == 1 || KIND == 3 ? 8 : 4);
+  return cudaFuncSetAttribute(fwt_rowbits_kernel<S, KIND>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+// Contiguous tiles of 2^TB elements transforming a run-time range of their bits.
+template <int DT, int KIND, int LV, int TB>
+KernelEntry rowbits_entry() {
+  constexpr int EL = choose_el(TB, LV);
+  using S = Shape<TB, 0, TB, LV, TB - EL>;
+  KernelEntry e;
+  e.dtype = DT; e.kind = KIND_ROWBITS; e.K = TB; e.TB = TB; e.TS = 0; e.col_bytes = 0; e.tma = 0;
+  e.threads = S::NT;
+  e.smem = (size_t)(1u << TB) * (16 >> LV);
+  e.launch = &launch_rowbits<S, KIND>;
+  e.setup = &setup_rowbits<S, KIND>;
+  e.selfcheck = [] {
+    int f = 0;
+    for (int ts = 0; ts < TB; ++ts)  // every run-time range: the rounds partition it
+      for (int tk = 0; ts + tk <= TB; ++tk) {
+        uint32_t rm[3];
+        S::round_masks(ts, tk, rm);
+        uint32_t seen = 0;
+        bool ok = true;
+        for (int L = 1; L <= 3; ++L)
+          for (int h = 0; h < S::EL; ++h)
+            if ((rm[L - 1] >> h) & 1u) {
+              const uint32_t b = 1u << S::rbit(L, h);
+              ok &= !(seen & b);
+              seen |= b;
+            }
+        const uint32_t want = (tk == 0 ? 0u : ((1u << tk) - 1u)) << ts;
+        if (!ok || seen != want) {
+          if (f < 4) fprintf(stderr, "fwt_selfcheck rowbits TB=%d: range [%d, %d) not covered once\n", TB, ts, ts + tk);
+          ++f;
+        }
+      }
+    return f;
+  };
+  e.fn = (const void*)&fwt_rowbits_kernel<S, KIND>;
   return e;
 }
 
@@ -295,8 +348,11 @@ KernelEntry small_entry() {
 cudaError_t read_device_error_c32(unsigned int* out);
 cudaError_t read_device_error_c64(unsigned int* out);
 cudaError_t read_device_error_i32(unsigned int* out);
-void register_c32(std::vector<KernelEntry>& v);
-void register_c64(std::vector<KernelEntry>& v);
-void register_i32(std::vector<KernelEntry>& v);
+void register_rows_c32(std::vector<KernelEntry>& v);
+void register_rows_c64(std::vector<KernelEntry>& v);
+void register_rows_i32(std::vector<KernelEntry>& v);
+void register_cols_c32(std::vector<KernelEntry>& v);
+void register_cols_c64(std::vector<KernelEntry>& v);
+void register_cols_i32(std::vector<KernelEntry>& v);
 
 }  // namespace fwt

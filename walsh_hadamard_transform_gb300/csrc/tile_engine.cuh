@@ -92,6 +92,17 @@ struct Shape {
   static constexpr uint32_t RM1 = reg_mask(1, DONE1);
   static constexpr uint32_t RM2 = reg_mask(2, DONE2);
   static constexpr uint32_t RM3 = reg_mask(3, DONE3);
+  // The same three register masks for transformed tile bits [ts, ts+tk) given at
+  // run time (a transform on a sub-range of the index bits).
+  __host__ __device__ static constexpr void round_masks(int ts, int tk, uint32_t (&rm)[3]) {
+    const uint32_t tset = (tk <= 0 ? 0u : ((tk >= 32 ? 0u : (1u << tk)) - 1u)) << ts;
+    const uint32_t d1 = reg_elem_bits(1) & tset;
+    const uint32_t d2 = reg_elem_bits(2) & tset & ~d1;
+    const uint32_t d3 = reg_elem_bits(3) & tset & ~(d1 | d2);
+    rm[0] = reg_mask(1, d1);
+    rm[1] = reg_mask(2, d2);
+    rm[2] = reg_mask(3, d3);
+  }
   // swizzled shared-memory element offset of a tile index
   __host__ __device__ static constexpr uint32_t phys(uint32_t idx) {
     return (swz_chunk(idx >> LV) << LV) | (idx & (VEC - 1));
@@ -133,13 +144,14 @@ struct Shape {
   __host__ __device__ static constexpr uint32_t c3(int j) { return ((uint32_t)j << 5) << LV; }
 };
 
-// In-register butterflies over the register bits in MASK: pairs (r, r | 2^h) with
-// bit h of r clear become (a + b, a - b).
-template <uint32_t MASK, class A, int NE, typename U>
-__device__ __forceinline__ void butterflies(U (&x)[NE]) {
+// In-register butterflies over the register bits in `mask`: pairs (r, r | 2^h) with
+// bit h of r clear become (a + b, a - b).  A compile-time mask folds the tests
+// away; a run-time mask is uniform over the CTA, so its tests never diverge.
+template <class A, int NE, typename U>
+__device__ __forceinline__ void butterflies(U (&x)[NE], uint32_t mask) {
 #pragma unroll
   for (int h = 0; h < ilog2c(NE); ++h) {
-    if ((MASK >> h) & 1u) {
+    if ((mask >> h) & 1u) {
 #pragma unroll
       for (int r = 0; r < NE; ++r) {
         if (!((r >> h) & 1)) {
@@ -183,10 +195,11 @@ __device__ __forceinline__ void get_vec(const U* p, U (&x)[NE], int j) {
 // shared buffer; nothing may be pending on it on entry, and its last reads (the
 // L3 loads) are not yet fenced by a barrier on exit.
 template <class S, class A, typename U>
-__device__ __forceinline__ void tile_rounds(U (&x)[S::NE], U* sm) {
+__device__ __forceinline__ void tile_rounds(U (&x)[S::NE], U* sm, uint32_t rm1 = S::RM1,
+                                            uint32_t rm2 = S::RM2, uint32_t rm3 = S::RM3) {
   const uint32_t t = threadIdx.x;
   uint32_t tab[8];
-  butterflies<S::RM1, A>(x);
+  butterflies<A>(x, rm1);
   // L1 -> shared (16-byte vectors)
   S::table1(t, tab);
 #pragma unroll
@@ -196,7 +209,7 @@ __device__ __forceinline__ void tile_rounds(U (&x)[S::NE], U* sm) {
   S::table2(t, tab);
 #pragma unroll
   for (int r = 0; r < S::NE; ++r) x[r] = sm[tab[S::h2(r)] + S::c2(r)];
-  butterflies<S::RM2, A>(x);
+  butterflies<A>(x, rm2);
   __syncthreads();
   // L2 -> shared (scalars)
 #pragma unroll
@@ -206,7 +219,7 @@ __device__ __forceinline__ void tile_rounds(U (&x)[S::NE], U* sm) {
   S::table3(t, tab);
 #pragma unroll
   for (int j = 0; j < S::NV; ++j) get_vec<U, S::VEC>(sm + tab[S::h3(j)] + S::c3(j), x, j);
-  butterflies<S::RM3, A>(x);
+  butterflies<A>(x, rm3);
 }
 
 }  // namespace fwt
