@@ -69,6 +69,8 @@ class Oracle:
         lib.oracle_fwt_bits_u32.argtypes = [up, up, ctypes.c_int, i64, ctypes.c_int, ctypes.c_int,
                                             ctypes.c_int]
         lib.oracle_fwt_bits_u32.restype = ctypes.c_int
+        lib.oracle_phase_fwt_f64.argtypes = [dp, dp, dp, i64, dp, dp, ctypes.c_int, i64, ctypes.c_int]
+        lib.oracle_phase_fwt_f64.restype = ctypes.c_int
         lib.oracle_fwt_entry_f64.argtypes = [dp, ctypes.c_int, i64, ctypes.c_int]
         lib.oracle_fwt_entry_f64.restype = ctypes.c_double
         lib.oracle_fwt_entry_u32.argtypes = [up, ctypes.c_int, i64]
@@ -151,6 +153,26 @@ class Oracle:
         out_im = None if im is None else self.fwt(im, normalize, nthreads)
         return self.fwt(re, normalize, nthreads), out_im
 
+    def phase_fwt(self, re, im, theta, normalize: bool = True):
+        """y = s * H (e^{i theta} . x) for split complex rows; ``theta`` has one row
+        per vector, or a single row shared by all vectors.  Returns float64 (re, im)."""
+        re = np.ascontiguousarray(re, dtype=np.float64)
+        im = np.ascontiguousarray(im, dtype=np.float64)
+        th = np.ascontiguousarray(np.atleast_2d(theta), dtype=np.float64)
+        n = self._n_of(re.shape[-1])
+        count = re.size // re.shape[-1] if re.size else 0
+        stride = 0 if th.shape[0] == 1 else re.shape[-1]
+        if th.shape[-1] != re.shape[-1] or (stride and th.shape[0] != count):
+            raise ValueError("theta must have one row per vector or a single shared row")
+        out_r, out_i = np.empty_like(re), np.empty_like(im)
+        dp = ctypes.POINTER(ctypes.c_double)
+        rc = self.lib.oracle_phase_fwt_f64(re.ctypes.data_as(dp), im.ctypes.data_as(dp),
+                                           th.ctypes.data_as(dp), stride, out_r.ctypes.data_as(dp),
+                                           out_i.ctypes.data_as(dp), n, count, int(bool(normalize)))
+        if rc:
+            raise RuntimeError(f"oracle_phase_fwt_f64 failed ({rc})")
+        return out_r, out_i
+
     # -- single entries from the definition ----------------------------------------
     def entry(self, vec, k: int, normalize: bool = True):
         """y[k] of one vector from the popc definition (compensated sum for floats)."""
@@ -193,6 +215,10 @@ def fwt_complex(re, im, normalize: bool = True, nthreads: int = 1):
 
 def fwt_bits(x, lo: int, nbits: int, normalize: bool = True, nthreads: int = 1) -> np.ndarray:
     return default().fwt_bits(x, lo, nbits, normalize, nthreads)
+
+
+def phase_fwt(re, im, theta, normalize: bool = True):
+    return default().phase_fwt(re, im, theta, normalize)
 
 
 def entry(vec, k: int, normalize: bool = True):

@@ -188,6 +188,39 @@ int oracle_fwt_bits_u32(const uint32_t* x, uint32_t* y, int n, int64_t count, in
 }
 
 /* Parity of popc(v): XOR-fold the 64 bits down to one. */
+/* IQP-style encoding step: each amplitude is first multiplied by the phase
+ * e^{i theta} (theta[b * theta_stride + i] for vector b), then the complex vector
+ * is transformed: y = s * H (e^{i theta} . x).  The phase step is the diagonal
+ * before the transform in "[QDP] [feature] Pr4 kronecker fwt" (IQP encoding,
+ * "IQP shared-mem fused" row of the benchmark table); the pages do not give the
+ * angle function, so theta is an input.  cos and sin from the C library, in
+ * double; then the same butterfly network as oracle_fwt_f64 on each part. */
+int oracle_phase_fwt_f64(const double* re, const double* im, const double* theta,
+                         int64_t theta_stride, double* re_out, double* im_out, int n,
+                         int64_t count, int normalize) {
+  if (n < 0 || n > 40 || count < 0) return 1;
+  const int64_t N = (int64_t)1 << n;
+  const double s = oracle_scale(n, normalize);
+  for (int64_t b = 0; b < count; ++b) {
+    const double* xr = re + b * N;
+    const double* xi = im + b * N;
+    const double* th = theta + b * theta_stride;
+    double* yr = re_out + b * N;
+    double* yi = im_out + b * N;
+    for (int64_t i = 0; i < N; ++i) {
+      const double c = cos(th[i]), sn = sin(th[i]);
+      const double r = xr[i] * c - xi[i] * sn;
+      const double m = xr[i] * sn + xi[i] * c;
+      yr[i] = r;
+      yi[i] = m;
+    }
+    butterfly_f64(yr, N);
+    butterfly_f64(yi, N);
+    for (int64_t k = 0; k < N; ++k) { yr[k] *= s; yi[k] *= s; }
+  }
+  return 0;
+}
+
 static int popc_parity(uint64_t v) {
   v ^= v >> 32; v ^= v >> 16; v ^= v >> 8; v ^= v >> 4; v ^= v >> 2; v ^= v >> 1;
   return (int)(v & 1u);

@@ -224,6 +224,41 @@ def pin_bit_range(orc):
         assert np.array_equal(twice, ((xi.astype(np.int64) << 3) % (1 << 32)).astype(np.uint32).view(np.int32))
 
 
+def pin_phase_then_transform(orc):
+    """y = s H (e^{i theta} . x): dense complex product for n <= 8; theta = 0 is the
+    plain transform; a constant phase commutes with H; theta = pi/2 multiplies by i;
+    |e^{i theta}| = 1 keeps the norm (Parseval)."""
+    rng = np.random.default_rng(29)
+    for n in (0, 1, 3, 8):
+        re, im = rng.standard_normal((2, 2, 1 << n))
+        th = rng.uniform(-np.pi, np.pi, size=(2, 1 << n))
+        H = dense.hadamard_popc(n).astype(np.float64) * 2.0 ** (-n / 2.0)
+        z = (re + 1j * im) * np.exp(1j * th)
+        ref = z @ H.T
+        yr, yi = orc.phase_fwt(re, im, th, normalize=True)
+        assert np.linalg.norm((yr + 1j * yi) - ref) <= 1e-13 * np.linalg.norm(ref), f"dense n={n}"
+        shared = th[:1]
+        yr1, yi1 = orc.phase_fwt(re, im, shared, normalize=True)
+        ref1 = ((re + 1j * im) * np.exp(1j * shared)) @ H.T
+        assert np.linalg.norm((yr1 + 1j * yi1) - ref1) <= 1e-13 * np.linalg.norm(ref1), "shared theta"
+    n = 12
+    re, im = rng.standard_normal((2, 3, 1 << n))
+    yr, yi = orc.phase_fwt(re, im, np.zeros((1, 1 << n)), normalize=True)
+    assert _rel(yr, orc.fwt(re)) < 1e-15 and _rel(yi, orc.fwt(im)) < 1e-15, "theta = 0"
+    phi = 0.7
+    yr, yi = orc.phase_fwt(re, im, np.full((1, 1 << n), phi), normalize=True)
+    plain = orc.fwt(re) + 1j * orc.fwt(im)
+    assert np.linalg.norm((yr + 1j * yi) - np.exp(1j * phi) * plain) <= 1e-13 * np.linalg.norm(plain)
+    yr, yi = orc.phase_fwt(re, im, np.full((1, 1 << n), np.pi / 2), normalize=True)
+    assert _rel(yr, -orc.fwt(im)) < 1e-14 and _rel(yi, orc.fwt(re)) < 1e-14, "theta = pi/2"
+    th = rng.uniform(0, 2 * np.pi, size=(3, 1 << n))
+    yr, yi = orc.phase_fwt(re, im, th, normalize=True)
+    for b in range(3):
+        a = np.sqrt(np.sum(yr[b] ** 2 + yi[b] ** 2))
+        e = np.sqrt(np.sum(re[b] ** 2 + im[b] ** 2))
+        assert abs(a / e - 1) < 1e-14, "Parseval with phase"
+
+
 ORACLE_PINS = [
     pin_butterfly_vs_dense_float,
     pin_butterfly_vs_dense_int,
@@ -237,4 +272,5 @@ ORACLE_PINS = [
     pin_scale,
     pin_fp32_promotion,
     pin_bit_range,
+    pin_phase_then_transform,
 ]

@@ -27,6 +27,8 @@ MUTANTS = [
     ("int entry transposed sign", "if (popc_parity((uint64_t)(k & i))) acc -= x[i];",
      "if (!popc_parity((uint64_t)(k & i))) acc -= x[i];", 0),
     ("scale skipped", "if (jb->scale != 1.0)", "if (jb->scale == 12345.0)", 0),
+    ("phase rotation sign", "const double r = xr[i] * c - xi[i] * sn;", "const double r = xr[i] * c + xi[i] * sn;", 0),
+    ("phase uses cos for sin", "const double c = cos(th[i]), sn = sin(th[i]);", "const double c = cos(th[i]), sn = cos(th[i]);", 0),
     ("bit range starts one stage late", "for (int64_t h = (int64_t)1 << lo;",
      "for (int64_t h = (int64_t)2 << lo;", 0),
     ("bit range scale uses n", "oracle_scale(nbits, normalize), 0, nthreads, lo, nbits)",
