@@ -56,6 +56,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=sorted(STEP_WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--bits", default="",
                     help="LO,NBITS: time the transform over index bits [LO, LO+NBITS) only")
+    ap.add_argument("--phase", action="store_true",
+                    help="time the fused phase + transform (fp32 parts; random per-vector angles)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch of every part (small cases for profiling; 0 = as specified)")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -247,21 +249,37 @@ def run_ours(args):
     torch.cuda.synchronize(device)
 
     bits = tuple(int(v) for v in args.bits.split(",")) if args.bits else None
+    if args.phase:
+        parts_idx = [i for i, w in enumerate(parts) if w.dtype == "c32"]
+        if not parts_idx or bits is not None:
+            raise SystemExit("--phase needs an fp32 workload and no --bits")
+        parts = [parts[i] for i in parts_idx]
+        host = [host[i] for i in parts_idx]
+        dev_in = [dev_in[i] for i in parts_idx]
+        dev_out = [dev_out[i] for i in parts_idx]
+        gen = torch.Generator(device=device).manual_seed(rank_seed(11, rank))
+        thetas = [torch.rand(w.batch, w.N, device=device, generator=gen) * (2 * np.pi) for w in parts]
 
     def step():
-        for w, (a, b), (c, d) in zip(parts, dev_in, dev_out):
-            fwt.transform(a, b, c, d, normalize=w.normalize, bits=bits)
+        for pi, (w, (a, b), (c, d)) in enumerate(zip(parts, dev_in, dev_out)):
+            if args.phase:
+                fwt.phase_transform(a, b, thetas[pi], c, d, normalize=w.normalize)
+            else:
+                fwt.transform(a, b, c, d, normalize=w.normalize, bits=bits)
 
     names, owners = [], []  # one entry per pass launched by a step, and its part
     for pi, (w, (a, b), (c, d)) in enumerate(zip(parts, dev_in, dev_out)):
-        if bits is None:
+        if bits is None and not args.phase:
             part_names = pass_names(w, fwt)
-        else:  # count the passes of a bit-range transform from one traced call
+        else:  # count the passes of a bit-range or phase transform from one traced call
             tr = fwt.PassTrace([torch.cuda.Event(enable_timing=True) for _ in range(16)])
             with tr:
-                fwt.transform(a, b, c, d, normalize=w.normalize, bits=bits)
-            part_names = [f"{w.dtype} bits [{bits[0]}, {bits[0] + bits[1]}) pass {i + 1} (n={w.n})"
-                          for i in range(tr.count // 2)]
+                if args.phase:
+                    fwt.phase_transform(a, b, thetas[pi], c, d, normalize=w.normalize)
+                else:
+                    fwt.transform(a, b, c, d, normalize=w.normalize, bits=bits)
+            what = "phase+transform" if args.phase else f"bits [{bits[0]}, {bits[0] + bits[1]})"
+            part_names = [f"{w.dtype} {what} pass {i + 1} (n={w.n})" for i in range(tr.count // 2)]
         names += part_names
         owners += [pi] * len(part_names)
     launches_per_step = len(names)
@@ -309,6 +327,8 @@ def run_ours(args):
     for li, (nm, pi) in enumerate(zip(names, owners)):
         mean_ms = statistics.mean(per_kernel[li])
         algo = 2 * parts[pi].bytes_in  # every pass reads and writes the whole batch once
+        if args.phase and li == [i for i, o in enumerate(owners) if o == pi][0]:
+            algo += algo // 4  # the first pass also reads the angles (fp32, one per amplitude)
         kernels.append({"kernel": nm, "mean_ms": mean_ms, "total_ms": sum(per_kernel[li]),
                         "algo_bytes_per_launch": algo, "gbs": algo / (mean_ms * 1e-3) / 1e9})
     top = max(kernels, key=lambda k: k["total_ms"])
@@ -326,7 +346,8 @@ def run_ours(args):
         "data": "synthetic (seeded PCG64; Gaussian unit-L2 states / uniform ints, per the workload)",
         "config": {
             "workload": (args.workload if args.batch <= 0 else "%s (batch %d)" % (args.workload, args.batch))
-                        + ("" if bits is None else " bits [%d, %d)" % (bits[0], bits[0] + bits[1])),
+                        + ("" if bits is None else " bits [%d, %d)" % (bits[0], bits[0] + bits[1]))
+                        + (" phase+transform" if args.phase else ""),
             "parts": [{"name": w.name, "n": w.n, "batch": w.batch, "dtype": w.dtype,
                        "normalize": w.normalize, "factors": fwt.plan_factors(w.n, w.dtype)}
                       for w in parts],

@@ -106,6 +106,27 @@ int fwt_bits_c64(const double* re_in, const double* im_in, double* re_out, doubl
 int fwt_bits_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, int32_t* im_out,
                  int n, int64_t batch, int lo, int nbits, int normalize, fwt_stream_t stream);
 
+/*
+ * Diagonal phase, then transform (the IQP-encoding step: the state is multiplied
+ * by a diagonal of phases before the Hadamard layer; "[QDP] [feature] Pr4
+ * kronecker fwt", IQP shared-mem fused path):
+ *
+ *     y = s * H (e^{i theta} . x),   theta[b * theta_stride + i] for vector b,
+ *
+ * complex fp32, split re/im.  The pages do not give the angle function, so the
+ * angles are an input: a DEVICE array of fp32 radians, theta_stride elements
+ * between vectors (0: one row of 2^n angles shared by the batch; 2^n: one row per
+ * vector).  theta must be 16-byte aligned, theta_stride a multiple of 4 when
+ * n >= 2, and the angle array must not overlap the outputs.  Phases come from
+ * sincosf; the rotation is fused into the first pass (one read of x and theta,
+ * one write), later passes as in fwt_batched_c32.  The relative L2 error per
+ * vector stays within 2e-6 of the exact result.  Other arguments, in-place rules
+ * and errors as fwt_batched_c32 (both parts are required).
+ */
+int fwt_phase_c32(const float* re_in, const float* im_in, const float* theta,
+                  int64_t theta_stride, float* re_out, float* im_out, int n, int64_t batch,
+                  int normalize, fwt_stream_t stream);
+
 /* Static text for a status code (never NULL). */
 const char* fwt_status_string(int status);
 

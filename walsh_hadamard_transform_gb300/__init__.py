@@ -58,6 +58,8 @@ def library() -> ctypes.CDLL:
             f = getattr(lib, name)
             f.argtypes = [vp, vp, vp, vp, ci, i64, ci, ci, ci, vp]
             f.restype = ci
+        lib.fwt_phase_c32.argtypes = [vp, vp, vp, i64, vp, vp, ci, i64, ci, vp]
+        lib.fwt_phase_c32.restype = ci
         lib.fwt_status_string.argtypes = [ci]
         lib.fwt_status_string.restype = ctypes.c_char_p
         lib.fwt_last_cuda_error.argtypes = []
@@ -119,6 +121,49 @@ def fwt_bits_c64(re_in, im_in, re_out, im_out, n, batch, lo, nbits, normalize, s
 def fwt_bits_i32(re_in, im_in, re_out, im_out, n, batch, lo, nbits, normalize, stream) -> int:
     return library().fwt_bits_i32(re_in, im_in, re_out, im_out, n, batch, lo, nbits,
                                   int(normalize), stream)
+
+
+def fwt_phase_c32(re_in, im_in, theta, theta_stride, re_out, im_out, n, batch, normalize,
+                  stream) -> int:
+    return library().fwt_phase_c32(re_in, im_in, theta, theta_stride, re_out, im_out, n, batch,
+                                   int(normalize), stream)
+
+
+def phase_transform(re, im, theta, out_re=None, out_im=None, normalize: bool = True, stream=None):
+    """y = s * H (e^{i theta} . x) for fp32 CUDA tensors of shape (batch, 2^n).
+
+    ``theta`` holds fp32 angles: shape (batch, 2^n) (one row per vector) or (2^n,) /
+    (1, 2^n) (shared by the batch).  Returns (out_re, out_im)."""
+    import torch
+
+    if re.dtype != torch.float32 or im is None or im.dtype != torch.float32:
+        raise TypeError("phase_transform takes float32 re and im")
+    if theta.dtype != torch.float32 or not theta.is_cuda or not theta.is_contiguous():
+        raise ValueError("theta must be a contiguous float32 CUDA tensor")
+    batch, N = re.shape
+    n = int(N).bit_length() - 1
+    if N < 1 or (1 << n) != N:
+        raise ValueError(f"row length {N} is not a power of two")
+    th2 = theta.reshape(-1, N)
+    if th2.shape[0] not in (1, batch):
+        raise ValueError("theta must have one row per vector or one shared row")
+    stride = 0 if th2.shape[0] == 1 else N
+    if out_re is None:
+        out_re = torch.empty_like(re)
+    if out_im is None:
+        out_im = torch.empty_like(im)
+    for t in (re, im, out_re, out_im):
+        if t.shape != re.shape or t.device != re.device or not t.is_contiguous():
+            raise ValueError("re, im and outputs must be contiguous CUDA tensors of one shape")
+    if stream is None:
+        stream = torch.cuda.current_stream(re.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(re.device):
+        st = fwt_phase_c32(re.data_ptr(), im.data_ptr(), theta.data_ptr(), stride, out_re.data_ptr(),
+                           out_im.data_ptr(), n, batch, normalize, handle)
+    if st != FWT_OK:
+        raise FwtError(st, f"fwt_phase_c32(n={n}, batch={batch})")
+    return out_re, out_im
 
 
 def status_string(status: int) -> str:

@@ -195,6 +195,10 @@ bool overlaps(const void* a, const void* b, size_t bytes) {
   const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
   return x < y + bytes && y < x + bytes;
 }
+bool overlaps2(const void* a, size_t a_bytes, const void* b, size_t b_bytes) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + b_bytes && y < x + a_bytes;
+}
 
 // One launch of a pass kernel over the whole batch (or one chunk of it).
 struct PassSpec {
@@ -222,6 +226,20 @@ const KernelEntry* column_kernel(int dtype, int K, int L, const Plan& plan) {
   return nullptr;
 }
 
+// Column passes over bits [L, hi), in factors of at most 10 bits.
+bool column_passes(int dtype, int L, int hi, const Plan& plan, std::vector<PassSpec>& out) {
+  const int rest = hi - L;
+  const int nf = (rest + 9) / 10;
+  for (int f = 0; f < nf; ++f) {
+    const int K = rest / nf + (f < rest % nf ? 1 : 0);
+    const KernelEntry* e = column_kernel(dtype, K, L, plan);
+    if (!e) return false;
+    out.push_back(PassSpec{e, L, 0, 0});
+    L += K;
+  }
+  return true;
+}
+
 // Passes of the whole transform for a Kronecker plan (factor 0 = row pass).
 bool full_passes(int n, int dtype, const Plan& plan, std::vector<PassSpec>& out) {
   int L = 0;
@@ -237,43 +255,38 @@ bool full_passes(int n, int dtype, const Plan& plan, std::vector<PassSpec>& out)
   return L == n;
 }
 
-// Passes of the transform over index bits [lo, lo + k) only: bits below the
-// largest row tile go to one run-time bit-range row pass, the rest to column
-// passes of at most 10 bits each.
+// Passes of the transform over index bits [lo, lo + k) only.  From bit 0: a row
+// pass (then column passes above the row tile); from a higher bit: column passes
+// (rows 2^lo elements apart) when tile shapes exist for the factors, else a
+// run-time bit-range row pass for the low part and column passes above it.
 bool range_passes(int n, int dtype, int lo, int k, const Plan& plan, std::vector<PassSpec>& out) {
   const int rmax = max_row_bits(dtype);
   const int hi = lo + k;
   if (lo == 0 && k == n) return full_passes(n, dtype, plan, out);
-  if (lo == 0 && k >= 3 && k <= rmax) {  // the low k bits: a plain row pass
-    const KernelEntry* e = find_kernel(dtype, KIND_ROW, k);
-    if (!e) return false;
-    out.push_back(PassSpec{e, 0, 0, 0});
-    return true;
-  }
-  if (hi <= rmax || k == 0) {
-    const int tb = std::max(hi, 10);
-    const KernelEntry* e = find_kernel(dtype, KIND_ROWBITS, std::min(tb, rmax));
+  if (k == 0 || (hi <= rmax && (lo > 0 || k <= 2))) {  // one run-time bit-range row pass
+    const KernelEntry* e = find_kernel(dtype, KIND_ROWBITS, std::min(std::max(hi, 10), rmax));
     if (!e) return false;
     out.push_back(PassSpec{e, 0, lo, k});
+    if (lo > 0 && k > 0) {  // prefer column passes when every factor has a tile shape
+      std::vector<PassSpec> cols;
+      if (column_passes(dtype, lo, hi, plan, cols)) out.swap(cols);
+    }
     return true;
   }
-  int L = lo;
-  if (lo < rmax) {  // bits [lo, rmax) in row tiles of 2^rmax elements
-    const KernelEntry* e = find_kernel(dtype, KIND_ROWBITS, rmax);
+  if (lo == 0) {  // row pass over the low bits, column passes above
+    const int k0 = std::min(k, std::min(rmax, 13));
+    const KernelEntry* e = find_kernel(dtype, KIND_ROW, k0);
     if (!e) return false;
-    out.push_back(PassSpec{e, 0, lo, rmax - lo});
-    L = rmax;
+    out.push_back(PassSpec{e, 0, 0, 0});
+    return k0 == k || column_passes(dtype, k0, hi, plan, out);
   }
-  const int rest = hi - L;
-  const int nf = (rest + 9) / 10;
-  for (int f = 0; f < nf; ++f) {
-    const int K = rest / nf + (f < rest % nf ? 1 : 0);
-    const KernelEntry* e = column_kernel(dtype, K, L, plan);
-    if (!e) return false;
-    out.push_back(PassSpec{e, L, 0, 0});
-    L += K;
-  }
-  return true;
+  if (column_passes(dtype, lo, hi, plan, out)) return true;
+  out.clear();
+  const int top = std::min(hi, rmax);  // bits [lo, top) in row tiles of 2^rmax elements
+  const KernelEntry* e = find_kernel(dtype, KIND_ROWBITS, rmax);
+  if (!e) return false;
+  out.push_back(PassSpec{e, 0, lo, top - lo});
+  return top == hi || column_passes(dtype, top, hi, plan, out);
 }
 
 int check_arrays(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out,
@@ -416,6 +429,89 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
   return FWT_OK;
 }
 
+// y = s * H (e^{i theta} . x), fp32: a fused phase + row pass over the low
+// min(n, 13) bits, then in-place column passes over the rest.
+int run_phase(const float* re_in, const float* im_in, const float* theta, int64_t theta_stride,
+              float* re_out, float* im_out, int n, int64_t batch, int normalize,
+              cudaStream_t stream) {
+  if (n < 0 || n > 30 || batch < 0 || theta_stride < 0) return FWT_ERR_INVALID_ARG;
+  if (batch == 0) return FWT_OK;
+  if (!im_in || !im_out || !theta) return FWT_ERR_INVALID_ARG;
+  bool has_im = false;
+  int st = check_arrays(FWT_C32, re_in, im_in, re_out, im_out, n, batch, has_im);
+  if (st != FWT_OK) return st;
+  if ((uintptr_t)theta & 15u) return FWT_ERR_MISALIGNED;
+  if (n >= 2 && theta_stride % 4 != 0) return FWT_ERR_MISALIGNED;  // 16-byte angle vectors
+  const long long th_elems = (theta_stride == 0 ? 0 : (long long)(batch - 1)) * theta_stride + (1ll << n);
+  const size_t th_bytes = (size_t)th_elems * 4;
+  const size_t bytes = (size_t)((long long)batch << n) * 4;
+  // the angles are read while the outputs are written: no overlap (either way round)
+  if (overlaps2(theta, th_bytes, re_out, bytes) || overlaps2(theta, th_bytes, im_out, bytes))
+    return FWT_ERR_INVALID_ARG;
+  cudaError_t err = ensure_device();
+  if (err != cudaSuccess) {
+    g_last_cuda_error = (int)err;
+    return FWT_ERR_CUDA;
+  }
+  Plan plan = default_plan(n, FWT_C32);
+  if (plan.tma && !tensor_map_encoder()) plan.tma = 0;
+  const int k1 = std::min(n, 13);
+  std::vector<PassSpec> passes;
+  const KernelEntry* e0 = find_kernel(FWT_C32, KIND_PHASE, k1);
+  if (!e0) return FWT_ERR_UNSUPPORTED;
+  passes.push_back(PassSpec{e0, 0, 0, 0});
+  if (n > k1 && !column_passes(FWT_C32, k1, n, plan, passes)) return FWT_ERR_UNSUPPORTED;
+
+  PassParams p{};
+  const double s = n % 2 == 0 ? std::ldexp(1.0, -n / 2) : std::ldexp(1.0, -(n - 1) / 2) / std::sqrt(2.0);
+  p.scale_f64 = s;
+  p.scale_f32 = (float)s;
+  p.scale_exp = -(n / 2);
+  p.scale_half = n % 2;
+  p.rsqrt2_q64 = rsqrt2_q64();
+  p.theta = theta;
+  p.theta_stride = theta_stride;
+  p.n = n;
+  const long long elems = (long long)batch << n;
+  p.comp_elems = elems;
+  const int npass = (int)passes.size();
+  for (int f = 0; f < npass; ++f) {
+    const KernelEntry* e = passes[f].e;
+    long long tiles;
+    if (e->kind == KIND_PHASE && e->K <= 2) tiles = ((elems >> e->K) + 255) / 256;
+    else if (e->kind == KIND_COL) tiles = elems >> e->TB;
+    else tiles = (elems + (1ll << e->TB) - 1) >> e->TB;
+    if (tiles > INT_MAX) return FWT_ERR_UNSUPPORTED;
+    p.in[0] = f == 0 ? (const void*)re_in : re_out;
+    p.in[1] = f == 0 ? (const void*)im_in : im_out;
+    p.out[0] = re_out;
+    p.out[1] = im_out;
+    p.stride_log = passes[f].L;
+    const bool last = f == npass - 1;
+    p.do_scale = (normalize && last) ? 1 : 0;
+    p.ld_policy = 1;
+    p.st_policy = last ? 1 : 0;
+    const bool traced = g_trace_count + 2 <= g_trace_capacity;
+    if (traced) {
+      err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count], stream);
+      if (err != cudaSuccess) {
+        g_last_cuda_error = (int)err;
+        return FWT_ERR_CUDA;
+      }
+    }
+    err = e->launch(p, tiles, 2, stream);
+    if (err == cudaSuccess && traced) {
+      err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count + 1], stream);
+      g_trace_count += 2;
+    }
+    if (err != cudaSuccess) {
+      g_last_cuda_error = (int)err;
+      return FWT_ERR_CUDA;
+    }
+  }
+  return FWT_OK;
+}
+
 }  // namespace
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -471,6 +567,13 @@ int fwt_bits_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, in
                  int n, int64_t batch, int lo, int nbits, int normalize, fwt_stream_t stream) {
   return fwt::run(FWT_I32, re_in, im_in, re_out, im_out, n, batch, lo, nbits, normalize,
                   (cudaStream_t)stream);
+}
+
+int fwt_phase_c32(const float* re_in, const float* im_in, const float* theta,
+                  int64_t theta_stride, float* re_out, float* im_out, int n, int64_t batch,
+                  int normalize, fwt_stream_t stream) {
+  return fwt::run_phase(re_in, im_in, theta, theta_stride, re_out, im_out, n, batch, normalize,
+                        (cudaStream_t)stream);
 }
 
 const char* fwt_status_string(int status) {

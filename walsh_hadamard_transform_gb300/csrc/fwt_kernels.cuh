@@ -51,6 +51,9 @@ struct PassParams {
   int ld_policy;         // L2 eviction priority of the loads: 0 normal, 1 first, 2 last
   int st_policy;         // ... and of the stores
   int bits_lo, bits_k;   // run-time bit-range tiles: transformed tile bits [lo, lo + k)
+  const float* theta;    // phase pass: angles, theta[b * theta_stride + i]
+  long long theta_stride;
+  int n;                 // phase pass: log2 of the vector length
 };
 
 // ---- arithmetic policies ----------------------------------------------------------
@@ -490,6 +493,84 @@ __global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
   __shared__ __align__(8) uint64_t bar;
   TmaMover<S> mv(tp, smem_raw, &bar);
   tile_body<S, KIND>(tp.p, smem_raw, mv, StaticBits<S>(tp.p));
+}
+
+// ---- fused diagonal phase + transform (first pass, fp32) ----------------------------
+// The first pass of y = s * H (e^{i theta} . x): each CTA loads the real part,
+// the imaginary part and the angles of one row tile, rotates every amplitude by
+// its phase (sincosf), and transforms both rotated parts in turn through the same
+// shared buffer.  Later passes (if any) are ordinary column passes.
+template <class S>
+__global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
+    fwt_phase_row_kernel(const PassParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  float* sm = reinterpret_cast<float*>(smem_raw);
+  const auto m = TileMap<S, false, true>::make(p, (long long)blockIdx.x);
+  const float* in_re = static_cast<const float*>(p.in[0]);
+  const float* in_im = static_cast<const float*>(p.in[1]);
+  const unsigned long long pol = l2_policy(p.ld_policy);
+  const long long vmask = (1ll << p.n) - 1;
+  float xr[S::NE], xi[S::NE];
+#pragma unroll
+  for (int j = 0; j < S::NV; ++j) {
+    const uint32_t u = S::idx1(threadIdx.x, j * S::VEC);
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a, th = a;
+    if (m.in_range(u)) {
+      const long long g = m.off(u);
+      a = ldg16<float>(in_re + g, pol);
+      b = ldg16<float>(in_im + g, pol);
+      th = ldg16<float>(p.theta + (g >> p.n) * p.theta_stride + (g & vmask), pol);
+    }
+    const float* pa = reinterpret_cast<const float*>(&a);
+    const float* pb = reinterpret_cast<const float*>(&b);
+    const float* pt = reinterpret_cast<const float*>(&th);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float sn, cs;
+      sincosf(pt[i], &sn, &cs);
+      xr[j * 4 + i] = pa[i] * cs - pb[i] * sn;
+      xi[j * 4 + i] = pa[i] * sn + pb[i] * cs;
+    }
+  }
+  tile_rounds<S, ArithF32>(xr, sm);
+  if (p.do_scale) {
+#pragma unroll
+    for (int r = 0; r < S::NE; ++r) xr[r] *= p.scale_f32;
+  }
+  store_tile<S>(static_cast<float*>(p.out[0]), m, xr, p.st_policy);
+  __syncthreads();  // the buffer's last reads (layout L3) are done
+  tile_rounds<S, ArithF32>(xi, sm);
+  if (p.do_scale) {
+#pragma unroll
+    for (int r = 0; r < S::NE; ++r) xi[r] *= p.scale_f32;
+  }
+  store_tile<S>(static_cast<float*>(p.out[1]), m, xi, p.st_policy);
+}
+
+// The same for vectors of 2^NL <= 4 elements: one thread per vector.
+template <int NL>
+__global__ void __launch_bounds__(256) fwt_phase_small_kernel(const PassParams p) {
+  const long long row = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= (p.comp_elems >> NL)) return;
+  const float* in_re = static_cast<const float*>(p.in[0]);
+  const float* in_im = static_cast<const float*>(p.in[1]);
+  float xr[1 << NL], xi[1 << NL];
+#pragma unroll
+  for (int i = 0; i < (1 << NL); ++i) {
+    float sn, cs;
+    sincosf(p.theta[row * p.theta_stride + i], &sn, &cs);
+    const float a = in_re[(row << NL) + i], b = in_im[(row << NL) + i];
+    xr[i] = a * cs - b * sn;
+    xi[i] = a * sn + b * cs;
+  }
+  butterflies<ArithF32>(xr, (1u << NL) - 1u);
+  butterflies<ArithF32>(xi, (1u << NL) - 1u);
+  const float s = p.do_scale ? p.scale_f32 : 1.0f;
+#pragma unroll
+  for (int i = 0; i < (1 << NL); ++i) {
+    static_cast<float*>(p.out[0])[(row << NL) + i] = xr[i] * s;
+    static_cast<float*>(p.out[1])[(row << NL) + i] = xi[i] * s;
+  }
 }
 
 // Vectors of 2^NL <= 4 elements: one thread per vector, plain arithmetic.

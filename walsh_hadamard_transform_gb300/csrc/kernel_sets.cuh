@@ -31,6 +31,16 @@ struct RowSet {
   }
 };
 
+// fp32 fused phase + transform first passes, K = 0 .. 13 (tiles of 32 elements a
+// thread: both rotated parts stay in registers).
+struct PhaseSet {
+  template <int... Ks>
+  static void add_k(std::vector<KernelEntry>& v, std::integer_sequence<int, Ks...>) {
+    (v.push_back(phase_entry<Ks>()), ...);
+  }
+  static void add(std::vector<KernelEntry>& v) { add_k(v, std::make_integer_sequence<int, 14>{}); }
+};
+
 // Column passes: for each segment width CB of 16..128 bytes, column factors K
 // with tiles of 2^10 .. 2^TBMAX elements, each with TMA staging and (from 32
 // bytes up) with vector loads; and the factors too short for those (K = 1 .. 4

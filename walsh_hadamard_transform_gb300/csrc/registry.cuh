@@ -12,7 +12,7 @@
 
 namespace fwt {
 
-enum PassKind { KIND_SMALL = 0, KIND_ROW = 1, KIND_COL = 2, KIND_ROWBITS = 3 };
+enum PassKind { KIND_SMALL = 0, KIND_ROW = 1, KIND_COL = 2, KIND_ROWBITS = 3, KIND_PHASE = 4 };
 
 struct KernelEntry {
   int dtype;  // FWT_C32 / FWT_C64 / FWT_I32
@@ -330,6 +330,47 @@ KernelEntry rowbits_entry() {
     return f;
   };
   e.fn = (const void*)&fwt_rowbits_kernel<S, KIND>;
+  return e;
+}
+
+template <class S>
+cudaError_t launch_phase_row(const PassParams& p, long long tiles, int, cudaStream_t st) {
+  const size_t smem = (size_t)4 << S::TB;
+  fwt_phase_row_kernel<S><<<(unsigned)tiles, S::NT, smem, st>>>(p);
+  return cudaGetLastError();
+}
+template <class S>
+cudaError_t setup_phase_row() {
+  return cudaFuncSetAttribute(fwt_phase_row_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)((size_t)4 << S::TB));
+}
+template <int NL>
+cudaError_t launch_phase_small(const PassParams& p, long long tiles, int, cudaStream_t st) {
+  fwt_phase_small_kernel<NL><<<(unsigned)tiles, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+// fp32 phase-then-transform first pass over bits [0, K) (K <= 2: a thread per vector).
+template <int K>
+KernelEntry phase_entry() {
+  KernelEntry e;
+  e.dtype = FWT_C32; e.kind = KIND_PHASE; e.K = K; e.TS = 0; e.col_bytes = 0; e.tma = 0;
+  if constexpr (K <= 2) {
+    e.TB = 0; e.threads = 256; e.smem = 0;
+    e.launch = &launch_phase_small<K>;
+    e.setup = &setup_none;
+    e.selfcheck = &selfcheck_none;
+    e.fn = (const void*)&fwt_phase_small_kernel<K>;
+  } else {
+    constexpr int TB = K > 10 ? K : 10;
+    constexpr int EL = choose_el(TB, 2);
+    using S = Shape<TB, 0, K, 2, TB - EL>;
+    e.TB = TB; e.threads = S::NT; e.smem = (size_t)4 << TB;
+    e.launch = &launch_phase_row<S>;
+    e.setup = &setup_phase_row<S>;
+    e.selfcheck = [] { return check_shape<S, false>("phase row"); };
+    e.fn = (const void*)&fwt_phase_row_kernel<S>;
+  }
   return e;
 }
 
