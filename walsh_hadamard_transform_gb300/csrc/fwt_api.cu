@@ -226,10 +226,12 @@ const KernelEntry* column_kernel(int dtype, int K, int L, const Plan& plan) {
   return nullptr;
 }
 
-// Column passes over bits [L, hi), in factors of at most 10 bits.
+// Column passes over bits [L, hi), in as few factors as the plan's segment width
+// allows (near-equal sizes).
 bool column_passes(int dtype, int L, int hi, const Plan& plan, std::vector<PassSpec>& out) {
   const int rest = hi - L;
-  const int nf = (rest + 9) / 10;
+  const int cmax = max_col_bits(dtype, plan.col_bytes);
+  const int nf = (rest + cmax - 1) / cmax;
   for (int f = 0; f < nf; ++f) {
     const int K = rest / nf + (f < rest % nf ? 1 : 0);
     const KernelEntry* e = column_kernel(dtype, K, L, plan);
@@ -264,7 +266,8 @@ bool range_passes(int n, int dtype, int lo, int k, const Plan& plan, std::vector
   const int hi = lo + k;
   if (lo == 0 && k == n) return full_passes(n, dtype, plan, out);
   if (k == 0 || (hi <= rmax && (lo > 0 || k <= 2))) {  // one run-time bit-range row pass
-    const KernelEntry* e = find_kernel(dtype, KIND_ROWBITS, std::min(std::max(hi, 10), rmax));
+    // tiles of at least 2^12 elements (128+ threads a CTA)
+    const KernelEntry* e = find_kernel(dtype, KIND_ROWBITS, std::min(std::max(hi, 12), rmax));
     if (!e) return false;
     out.push_back(PassSpec{e, 0, lo, k});
     if (lo > 0 && k > 0) {  // prefer column passes when every factor has a tile shape
