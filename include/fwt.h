@@ -189,6 +189,15 @@ int fwt_get_tma(void);
 int fwt_device_status(void);
 
 /*
+ * Self-test of the bounded device wait: enqueues on `stream` one CTA that waits
+ * on an mbarrier nobody arrives at (no copy targets it), so the wait gives up
+ * after about one second and records a timeout; afterwards fwt_device_status()
+ * returns FWT_ERR_TIMEOUT (and clears it).  Nothing is left in flight.  Returns
+ * FWT_OK when enqueued.
+ */
+int fwt_selftest_bounded_wait(fwt_stream_t stream);
+
+/*
  * L2 chunking of multi-pass transforms (tuning): when a plan has two or more
  * passes, the library runs all passes on one group of whole vectors before the
  * next group, so each intermediate is read back from L2 rather than DRAM.  A

@@ -279,3 +279,18 @@ def test_l2_chunked_schedules(dtype):
             assert np.array_equal(gre, ore)
     finally:
         fwt.set_l2_chunk_bytes(0)
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """A wait on an mbarrier nobody arrives at gives up after ~1 s, records a
+    timeout for fwt_device_status(), and leaves the context usable."""
+    import time
+
+    assert fwt.device_status() == fwt.FWT_OK
+    t = time.time()
+    assert fwt.selftest_bounded_wait() == fwt.FWT_OK
+    torch.cuda.synchronize()
+    assert 0.5 < time.time() - t < 30
+    assert fwt.device_status() == fwt.FWT_ERR_TIMEOUT
+    assert fwt.device_status() == fwt.FWT_OK  # cleared
+    _check("c32", 12, 2, True, seed=1)  # the context still works

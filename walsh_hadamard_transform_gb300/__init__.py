@@ -80,6 +80,8 @@ def library() -> ctypes.CDLL:
         lib.fwt_set_tma.restype = ci
         lib.fwt_get_tma.argtypes = []
         lib.fwt_get_tma.restype = ci
+        lib.fwt_selftest_bounded_wait.argtypes = [vp]
+        lib.fwt_selftest_bounded_wait.restype = ci
         lib.fwt_device_status.argtypes = []
         lib.fwt_device_status.restype = ci
         lib.fwt_set_l2_chunk_bytes.argtypes = [ctypes.c_longlong]
@@ -223,6 +225,11 @@ def tma() -> int:
 def device_status() -> int:
     """FWT_ERR_TIMEOUT if a kernel gave up a bounded TMA wait since the last call."""
     return library().fwt_device_status()
+
+
+def selftest_bounded_wait(stream=None) -> int:
+    """Enqueue the bounded-wait self-test (one CTA, ~1 s); see fwt_selftest_bounded_wait."""
+    return library().fwt_selftest_bounded_wait(stream)
 
 
 def set_l2_chunk_bytes(nbytes: int) -> None:

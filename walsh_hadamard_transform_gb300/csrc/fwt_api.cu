@@ -648,6 +648,16 @@ int fwt_get_tma(void) {
   return fwt::g_use_tma;
 }
 
+int fwt_selftest_bounded_wait(fwt_stream_t stream) {
+  cudaError_t err = fwt::ensure_device();
+  if (err == cudaSuccess) err = fwt::launch_bounded_wait_probe((cudaStream_t)stream);
+  if (err != cudaSuccess) {
+    fwt::g_last_cuda_error = (int)err;
+    return FWT_ERR_CUDA;
+  }
+  return FWT_OK;
+}
+
 int fwt_device_status(void) {
   unsigned int e[3] = {0, 0, 0};
   cudaError_t err = fwt::read_device_error_c32(&e[0]);

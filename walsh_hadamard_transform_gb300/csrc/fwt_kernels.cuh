@@ -329,11 +329,9 @@ __device__ __forceinline__ long long to_fixed(long long bits, int emax, int F) {
   if constexpr (RIGHT) {  // sh <= F - 52 <= 0: always a rounding right shift
     const int rs = min(-sh, 63);
     mag = (((m << 1) >> rs) + 1ull) >> 1;
-  } else if (sh >= 0) {
-    mag = m << sh;
-  } else {
-    const int rs = min(-sh, 63);
-    mag = (((m << 1) >> rs) + 1ull) >> 1;
+  } else {  // either way, without a divergent branch: (sh >= 0: rs = 0, exact)
+    const int rs = min(max(-sh, 0), 63);
+    mag = ((((m << 1) >> rs) + 1ull) >> 1) << max(sh, 0);
   }
   const unsigned long long neg = (unsigned long long)((long long)b >> 63);  // 0 or ~0
   return (long long)((mag ^ neg) - neg);

@@ -387,6 +387,7 @@ KernelEntry small_entry() {
 }
 
 cudaError_t read_device_error_c32(unsigned int* out);
+cudaError_t launch_bounded_wait_probe(cudaStream_t st);
 cudaError_t read_device_error_c64(unsigned int* out);
 cudaError_t read_device_error_i32(unsigned int* out);
 void register_rows_c32(std::vector<KernelEntry>& v);

@@ -50,15 +50,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
-// Waits for phase `parity` of the barrier, giving up after a bounded number of
-// tries (each suspends for up to ~1 us, so about 4 s in all).  On give-up it
-// records kErrTmaTimeout and returns false.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for phase `parity` of the barrier for at most about one second (global
+// timer, with an iteration cap as a backstop).  On give-up it records
+// kErrTmaTimeout and returns false.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < (1u << 22); ++i)
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1; i < (1u << 26); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0 && global_ns() - t0 > 1000000000ull) break;
+  }
   atomicOr(&g_device_error, kErrTmaTimeout);
   return false;
 }
+
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar, unsigned long long policy) {
