@@ -182,6 +182,24 @@ int fwt_set_tma(int mode);
 int fwt_get_tma(void);
 
 /*
+ * One-pass cluster transform (fp32 / int32): a vector of 2^14 .. 2^18 elements is
+ * spread over a thread-block cluster of 2 .. 16 CTAs; each CTA transforms the low
+ * bits of its slice on chip, and the top bits are transformed across the cluster
+ * through distributed shared memory, so the vector costs one HBM read and one
+ * write instead of two of each (two Kronecker passes).  mode 1 (default): for
+ * n = 15 and 16 (where it measured faster than the factor plans) when the device
+ * can hold such a cluster; 2: for every n from 14 to 18; 0: never (factor plans
+ * only).  Plans set with fwt_set_plan take precedence.  Returns FWT_OK or
+ * FWT_ERR_INVALID_ARG; fwt_get_cluster returns the mode.
+ */
+int fwt_set_cluster(int mode);
+int fwt_get_cluster(void);
+
+/* Tuning: L2 sector promotion (0, 64, 128 (default) or 256 bytes) of the TMA
+ * copies of column tiles.  Returns FWT_OK or FWT_ERR_INVALID_ARG. */
+int fwt_set_tma_l2_promotion(int bytes);
+
+/*
  * Device-side status: returns FWT_ERR_TIMEOUT if, since the last call, some kernel
  * gave up a bounded wait for a TMA copy (that tile was left unwritten), else
  * FWT_OK; clears the record.  Synchronises the device (it reads device memory).

@@ -88,7 +88,8 @@ def test_plans(lib):
             f = fwt.plan_factors(n, dt)
             assert sum(f) == n and 1 <= len(f) <= 3
             assert fwt.plan_passes(n, dt) == len(f)
-            assert (len(f) == 1) == (n <= rmax)
+            cluster_ok = dt != "c64" and 15 <= n <= 16  # one-pass cluster plans on a GPU
+            assert (len(f) == 1) == (n <= rmax) or (cluster_ok and len(f) == 1)
     assert fwt.plan_factors(24, "c32") == [14, 10]
     assert fwt.plan_factors(24, "c64") == [13, 11]
     assert lib.fwt_plan_passes(31, 0) == -1 and lib.fwt_plan_passes(10, 7) == -1
@@ -158,3 +159,12 @@ def test_bit_range_argument_errors_before_launch(lib, fn):
     assert f(a + 4, b, c, d, 8, 1, 0, 3, 0, None) == fwt.FWT_ERR_MISALIGNED
     assert f(a, b, b, d, 8, 1, 0, 3, 0, None) == fwt.FWT_ERR_INVALID_ARG   # re_out over im_in
     assert f(None, None, None, None, 8, 0, 0, 3, 0, None) == fwt.FWT_OK     # empty batch
+
+
+def test_cluster_setting(lib):
+    assert fwt.cluster() == fwt.CLUSTER_AUTO
+    fwt.set_cluster(fwt.CLUSTER_NEVER)
+    assert fwt.cluster() == fwt.CLUSTER_NEVER
+    with pytest.raises(fwt.FwtError):
+        fwt.set_cluster(5)
+    fwt.set_cluster(fwt.CLUSTER_AUTO)

@@ -294,3 +294,25 @@ def test_bounded_wait_gives_up_and_reports():
     assert fwt.device_status() == fwt.FWT_ERR_TIMEOUT
     assert fwt.device_status() == fwt.FWT_OK  # cleared
     _check("c32", 12, 2, True, seed=1)  # the context still works
+
+
+@pytest.mark.parametrize("dtype", ["c32", "i32"])
+def test_cluster_one_pass(dtype):
+    """n = 14..18 through the one-pass cluster kernels (forced from n = 14), in and
+    out of place, and equal to the factor plans (bit-exact for int32)."""
+    try:
+        for n in (14, 15, 16, 17, 18):
+            fwt.set_cluster(fwt.CLUSTER_FROM_14)
+            assert fwt.plan_passes(n, dtype) == 1
+            for inplace in (False, True):
+                _check(dtype, n, 3, dtype != "i32", seed=90 + n, inplace=inplace)
+            re, im = inputs.random_pair(n, 2, dtype, seed=n)
+            a = gpu_transform(re, im, dtype != "i32")
+            fwt.set_cluster(fwt.CLUSTER_NEVER)
+            b = gpu_transform(re, im, dtype != "i32")
+            if dtype == "i32":
+                assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+            else:
+                assert rel_err_per_vector(a[0], a[1], b[0], b[1]).max() < 4e-6
+    finally:
+        fwt.set_cluster(fwt.CLUSTER_AUTO)

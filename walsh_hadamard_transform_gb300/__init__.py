@@ -80,6 +80,12 @@ def library() -> ctypes.CDLL:
         lib.fwt_set_tma.restype = ci
         lib.fwt_get_tma.argtypes = []
         lib.fwt_get_tma.restype = ci
+        lib.fwt_set_cluster.argtypes = [ci]
+        lib.fwt_set_cluster.restype = ci
+        lib.fwt_get_cluster.argtypes = []
+        lib.fwt_get_cluster.restype = ci
+        lib.fwt_set_tma_l2_promotion.argtypes = [ci]
+        lib.fwt_set_tma_l2_promotion.restype = ci
         lib.fwt_selftest_bounded_wait.argtypes = [vp]
         lib.fwt_selftest_bounded_wait.restype = ci
         lib.fwt_device_status.argtypes = []
@@ -220,6 +226,28 @@ def set_tma(mode: int) -> None:
 
 def tma() -> int:
     return library().fwt_get_tma()
+
+
+CLUSTER_NEVER, CLUSTER_AUTO, CLUSTER_FROM_14 = 0, 1, 2
+
+
+def set_cluster(mode: int) -> None:
+    """One-pass cluster transforms of 2^14..2^18-element fp32/int32 vectors:
+    CLUSTER_AUTO (default: n = 15, 16), CLUSTER_FROM_14 (n = 14..18) or CLUSTER_NEVER."""
+    st = library().fwt_set_cluster(int(mode))
+    if st != FWT_OK:
+        raise FwtError(st, f"fwt_set_cluster({mode})")
+
+
+def cluster() -> int:
+    return library().fwt_get_cluster()
+
+
+def set_tma_l2_promotion(nbytes: int) -> None:
+    """L2 sector promotion of TMA column-tile copies: 0, 64, 128 (default) or 256 bytes."""
+    st = library().fwt_set_tma_l2_promotion(int(nbytes))
+    if st != FWT_OK:
+        raise FwtError(st, f"fwt_set_tma_l2_promotion({nbytes})")
 
 
 def device_status() -> int:

@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -37,15 +38,23 @@ const std::vector<KernelEntry>& table() {
   return t;
 }
 
+// Column kernels are also keyed by segment width and mover; cluster kernels by
+// their slice size (passed as col_bytes).
 const KernelEntry* find_kernel(int dtype, int kind, int K, int col_bytes = 0, int tma = 0) {
   for (const KernelEntry& e : table())
     if (e.dtype == dtype && e.kind == kind && e.K == K &&
-        (kind != KIND_COL || (e.col_bytes == col_bytes && e.tma == tma)))
+        (kind != KIND_COL || (e.col_bytes == col_bytes && e.tma == tma)) &&
+        (kind != KIND_CLUSTER || e.TB == col_bytes))
       return &e;
   return nullptr;
 }
 
 int elem_size(int dtype) { return dtype == FWT_C64 ? 8 : 4; }
+
+// Whether a cluster kernel can run on the current device (cached per device).
+std::mutex g_cap_mu;
+std::vector<std::vector<signed char>> g_cap;  // [device][table index]: -1 unknown, 0 no, 1 yes
+bool cluster_runnable(const KernelEntry* e);
 
 // ---- plans -----------------------------------------------------------------------
 // A plan is the list of Kronecker factors H_n = H_{f_last} (x) ... (x) H_{f_0}, each
@@ -56,6 +65,7 @@ struct Plan {
   int bits[3] = {0, 0, 0};
   int col_bytes = 128;  // width of the column passes' row segments
   int tma = 1;          // TMA-staged column passes: 0 never, 1 for K >= 10, 2 always
+  const KernelEntry* cluster = nullptr;  // one-pass cluster kernel instead of the factors
 };
 
 // TMA staging pays for column tiles with many rows (long strided walks); short
@@ -69,6 +79,7 @@ std::mutex g_plan_mu;
 Plan g_override[3][31];  // nf == 0: no override
 int g_col_bytes[3] = {64, 32, 64};  // default column segment width per dtype
 int g_use_tma = 1;                    // TMA-staged column passes: 0 never, 1 auto, 2 always
+int g_use_cluster = 1;                // one-pass cluster kernels: 0 never, 1 auto, 2 from n = 14
 
 int max_row_bits(int dtype) { return dtype == FWT_C64 ? 14 : 15; }
 // column factors available for a segment width: tiles of 2^10 .. 2^15 (2^14 fp64) elements
@@ -135,12 +146,30 @@ Plan default_plan(int n, int dtype) {
 }
 
 Plan get_plan(int n, int dtype) {
+  int mode;
   {
     std::lock_guard<std::mutex> lk(g_plan_mu);
     const Plan& o = g_override[dtype][n];
     if (o.nf > 0) return o;
+    mode = g_use_cluster;
   }
-  return default_plan(n, dtype);
+  Plan p = default_plan(n, dtype);
+  // a vector of 2^14 .. 2^18 4-byte elements in one pass on a thread-block cluster
+  // (slices of 2^14, else 2^15 or 2^13).  Measured on GB300 against the two-pass
+  // plans: faster for n = 15, 16 (clusters of 2 and 4 CTAs), even at 17, slower at
+  // 18 (16-CTA clusters), so the default uses it for n = 15, 16 only.
+  const int lo_n = mode == 2 ? 14 : 15, hi_n = mode == 2 ? 18 : 16;
+  if (dtype != FWT_C64 && mode > 0 && n >= lo_n && n <= hi_n) {
+    for (int tb : {14, 15, 13}) {
+      if (n - tb < 1 || n - tb > 4) continue;
+      const KernelEntry* e = find_kernel(dtype, KIND_CLUSTER, n, tb);
+      if (e && cluster_runnable(e)) {
+        p.cluster = e;
+        break;
+      }
+    }
+  }
+  return p;
 }
 
 // ---- per-device set-up -------------------------------------------------------------
@@ -177,8 +206,24 @@ cudaError_t ensure_device() {
   return cudaSuccess;
 }
 
+std::atomic<int> g_tma_promotion{128};
 std::once_flag g_encoder_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encoder = nullptr;
+
+bool cluster_runnable(const KernelEntry* e) {
+  int dev = 0;
+  if (!e->capacity || cudaGetDevice(&dev) != cudaSuccess) return false;
+  const size_t ix = (size_t)(e - table().data());
+  std::lock_guard<std::mutex> lk(g_cap_mu);
+  if ((int)g_cap.size() <= dev) g_cap.resize(dev + 1);
+  if (g_cap[dev].size() < table().size()) g_cap[dev].resize(table().size(), -1);
+  if (g_cap[dev][ix] < 0) {
+    const bool ok = e->setup() == cudaSuccess && e->capacity() > 0;
+    if (!ok) cudaGetLastError();
+    g_cap[dev][ix] = ok ? 1 : 0;
+  }
+  return g_cap[dev][ix] == 1;
+}
 
 // floor(2^64 / sqrt(2)) = floor(sqrt(2^127)), by bitwise integer square root.
 unsigned long long rsqrt2_q64() {
@@ -244,6 +289,10 @@ bool column_passes(int dtype, int L, int hi, const Plan& plan, std::vector<PassS
 
 // Passes of the whole transform for a Kronecker plan (factor 0 = row pass).
 bool full_passes(int n, int dtype, const Plan& plan, std::vector<PassSpec>& out) {
+  if (plan.cluster) {
+    out.push_back(PassSpec{plan.cluster, 0, 0, 0});
+    return true;
+  }
   int L = 0;
   for (int f = 0; f < plan.nf; ++f) {
     const int K = plan.bits[f];
@@ -328,14 +377,13 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
   if (st != FWT_OK) return st;
   const int esz = elem_size(dtype);
   const bool whole = lo == 0 && k == n;
-  Plan plan = whole ? get_plan(n, dtype) : default_plan(n, dtype);
-  if (whole && !plan_valid(n, dtype, plan)) return FWT_ERR_UNSUPPORTED;
-
   cudaError_t err = ensure_device();
   if (err != cudaSuccess) {
     g_last_cuda_error = (int)err;
     return FWT_ERR_CUDA;
   }
+  Plan plan = whole ? get_plan(n, dtype) : default_plan(n, dtype);
+  if (whole && !plan.cluster && !plan_valid(n, dtype, plan)) return FWT_ERR_UNSUPPORTED;
   if (plan.tma && !tensor_map_encoder()) plan.tma = 0;  // driver without the TMA encoder
   std::vector<PassSpec> passes;
   if (!range_passes(n, dtype, lo, k, plan, passes)) return FWT_ERR_UNSUPPORTED;
@@ -383,7 +431,7 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
         const KernelEntry* e = ps.e;
         long long tiles;
         if (e->kind == KIND_SMALL) tiles = ((elems >> e->K) + 255) / 256;
-        else if (e->kind == KIND_COL) tiles = elems >> e->TB;
+        else if (e->kind == KIND_COL || e->kind == KIND_CLUSTER) tiles = elems >> e->TB;
         else tiles = (elems + (1ll << e->TB) - 1) >> e->TB;
         if (tiles > INT_MAX) return FWT_ERR_UNSUPPORTED;
         p.comp_elems = elems;
@@ -517,6 +565,8 @@ int run_phase(const float* re_in, const float* im_in, const float* theta, int64_
 
 }  // namespace
 
+int tma_l2_promotion() { return g_tma_promotion.load(); }
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   std::call_once(g_encoder_once, [] {
     void* fn = nullptr;
@@ -595,7 +645,11 @@ int fwt_last_cuda_error(void) { return fwt::g_last_cuda_error; }
 
 int fwt_plan_factors(int n, int dtype, int* bits, int max_factors) {
   if (n < 0 || n > 30 || dtype < 0 || dtype > 2) return -1;
-  const fwt::Plan p = fwt::get_plan(n, dtype);
+  fwt::Plan p = fwt::get_plan(n, dtype);
+  if (p.cluster) {  // one pass over the whole vector
+    p.nf = 1;
+    p.bits[0] = n;
+  }
   for (int f = 0; f < p.nf && f < max_factors; ++f) bits[f] = p.bits[f];
   return p.nf;
 }
@@ -640,6 +694,24 @@ int fwt_set_tma(int mode) {
   if (mode < 0 || mode > 2) return FWT_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
   fwt::g_use_tma = mode;
+  return FWT_OK;
+}
+
+int fwt_set_cluster(int mode) {
+  if (mode < 0 || mode > 2) return FWT_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
+  fwt::g_use_cluster = mode;
+  return FWT_OK;
+}
+
+int fwt_get_cluster(void) {
+  std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
+  return fwt::g_use_cluster;
+}
+
+int fwt_set_tma_l2_promotion(int bytes) {
+  if (bytes != 0 && bytes != 64 && bytes != 128 && bytes != 256) return FWT_ERR_INVALID_ARG;
+  fwt::g_tma_promotion.store(bytes);
   return FWT_OK;
 }
 

@@ -493,6 +493,102 @@ __global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
   tile_body<S, KIND>(tp.p, smem_raw, mv, StaticBits<S>(tp.p));
 }
 
+// ---- one-pass transform of a vector spread over a thread-block cluster -----------------
+// A vector of 2^n elements, n = TB + CL, is held by a cluster of 2^CL CTAs, CTA r
+// owning the contiguous slice [r 2^TB, (r+1) 2^TB).  Each CTA transforms the low TB
+// index bits of its slice with the tile engine, writes the result into its shared
+// memory in natural order, and after a cluster barrier transforms the top CL bits
+// across the cluster: CTA r reads, for its share of slice positions i, the element
+// at i of every CTA's slice from distributed shared memory (ld.shared::cluster),
+// runs the CL butterfly stages in registers and writes the 2^CL outputs.  The whole
+// transform costs one HBM read and one write of each element (the second Kronecker
+// factor moves over the cluster's shared memory instead of HBM).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// 16-byte load from the shared memory of CTA `rank` of the cluster, at the same
+// offset as `local` in this CTA.
+__device__ __forceinline__ uint4 ld_dsmem16(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+
+template <class S, int KIND, int CL>
+__global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
+    fwt_cluster_kernel(const PassParams p) {
+  using T = typename std::conditional<KIND == 0, float, uint32_t>::type;
+  using A = typename std::conditional<KIND == 0, ArithF32, ArithU32>::type;
+  constexpr int C = 1 << CL;
+  constexpr int M = 1 << (S::TB - CL);  // slice positions each CTA finishes
+  constexpr int GROUPS = M / S::VEC / S::NT;  // 16-byte positions a thread finishes
+  static_assert(GROUPS >= 1, "each thread finishes at least one 16-byte position");
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  T* sm = reinterpret_cast<T*>(smem_raw);
+  const uint32_t t = threadIdx.x;
+  const uint32_t rank = cluster_ctarank();
+  const long long vec = (long long)blockIdx.x >> CL;
+  const bool im = blockIdx.y != 0;
+  const T* in = static_cast<const T*>(im ? p.in[1] : p.in[0]);
+  T* out = static_cast<T*>(im ? p.out[1] : p.out[0]);
+  const long long vbase = vec << (S::TB + CL);
+
+  // low TB bits of the slice, in the tile engine
+  TileMap<S, false, false> m;
+  m.base = vbase + ((long long)rank << S::TB);
+  m.L = 0;
+  m.valid = 0;
+  T x[S::NE];
+  load_tile<S>(in, m, x, p.ld_policy);
+  tile_rounds<S, A>(x, sm);
+  __syncthreads();  // the engine's last reads of the buffer are done
+#pragma unroll
+  for (int j = 0; j < S::NV; ++j) put_vec<T, S::VEC>(sm + S::idx3(t, j * S::VEC), x, j);
+  cluster_sync_all();  // every slice is in its CTA's shared memory
+
+  // top CL bits across the cluster
+  const unsigned long long pol = l2_policy(p.st_policy);
+#pragma unroll
+  for (int q = 0; q < GROUPS; ++q) {
+    const uint32_t i = rank * M + (t + q * S::NT) * S::VEC;  // slice position of this group
+    T y[C * S::VEC];
+#pragma unroll
+    for (int r = 0; r < C; ++r) {
+      const uint4 v = ld_dsmem16(sm + i, (uint32_t)r);
+      const T* pv = reinterpret_cast<const T*>(&v);
+#pragma unroll
+      for (int e = 0; e < S::VEC; ++e) y[r * S::VEC + e] = pv[e];
+    }
+    butterflies<A>(y, (uint32_t)(C - 1) << S::LV);
+    if constexpr (KIND == 0) {
+      if (p.do_scale) {
+#pragma unroll
+        for (int e = 0; e < C * S::VEC; ++e) y[e] = y[e] * p.scale_f32;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < C; ++r) {
+      typename Vec16<T>::type v;
+      T* pv = reinterpret_cast<T*>(&v);
+#pragma unroll
+      for (int e = 0; e < S::VEC; ++e) pv[e] = y[r * S::VEC + e];
+      stg16<T>(out + vbase + ((long long)r << S::TB) + i, v, pol);
+    }
+  }
+  cluster_sync_all();  // no CTA leaves while others still read its shared memory
+}
+
 // ---- fused diagonal phase + transform (first pass, fp32) ----------------------------
 // The first pass of y = s * H (e^{i theta} . x): each CTA loads the real part,
 // the imaginary part and the angles of one row tile, rotates every amplitude by

@@ -31,6 +31,22 @@ struct RowSet {
   }
 };
 
+// One-pass cluster transforms for 4-byte types: slices of 2^13, 2^14 or 2^15
+// elements on clusters of 2 .. 16 CTAs (n = 14 .. 18).
+template <int DT, int KIND>
+struct ClusterSet {
+  static void add(std::vector<KernelEntry>& v) {
+    v.push_back(cluster_entry<DT, KIND, 14, 1>());
+    v.push_back(cluster_entry<DT, KIND, 14, 2>());
+    v.push_back(cluster_entry<DT, KIND, 14, 3>());
+    v.push_back(cluster_entry<DT, KIND, 14, 4>());
+    v.push_back(cluster_entry<DT, KIND, 13, 1>());
+    v.push_back(cluster_entry<DT, KIND, 13, 2>());
+    v.push_back(cluster_entry<DT, KIND, 13, 3>());
+    v.push_back(cluster_entry<DT, KIND, 15, 3>());
+  }
+};
+
 // fp32 fused phase + transform first passes, K = 0 .. 13 (tiles of 32 elements a
 // thread: both rotated parts stay in registers).
 struct PhaseSet {

@@ -12,7 +12,14 @@
 
 namespace fwt {
 
-enum PassKind { KIND_SMALL = 0, KIND_ROW = 1, KIND_COL = 2, KIND_ROWBITS = 3, KIND_PHASE = 4 };
+enum PassKind {
+  KIND_SMALL = 0,
+  KIND_ROW = 1,
+  KIND_COL = 2,
+  KIND_ROWBITS = 3,
+  KIND_PHASE = 4,
+  KIND_CLUSTER = 5  // one pass over a vector spread across a thread-block cluster
+};
 
 struct KernelEntry {
   int dtype;  // FWT_C32 / FWT_C64 / FWT_I32
@@ -28,6 +35,7 @@ struct KernelEntry {
   cudaError_t (*setup)();  // per-device attributes; call with the device current
   int (*selfcheck)();      // host-only index-map and bank-conflict check
   const void* fn;
+  int (*capacity)() = nullptr;  // cluster kernels: resident clusters (device current)
 };
 
 // Elements per thread for a tile of 2^TB elements: enough registers that the
@@ -200,6 +208,8 @@ inline int selfcheck_none() { return 0; }
 
 // The driver's tensor-map encoder, resolved once at run time (nullptr if absent).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+// L2 sector promotion of TMA column tiles, in bytes (0, 64, 128 or 256).
+int tma_l2_promotion();
 
 template <class S, int KIND>
 cudaError_t launch_col_tma(const PassParams& p, long long tiles, int ncomp, cudaStream_t st) {
@@ -219,9 +229,14 @@ cudaError_t launch_col_tma(const PassParams& p, long long tiles, int ncomp, cuda
   tp.p = p;
   for (int c = 0; c < ncomp; ++c) {
     if (p.in[c] != p.out[c]) return cudaErrorInvalidValue;  // column passes run in place
+    const int promo = tma_l2_promotion();
+    const CUtensorMapL2promotion prom = promo == 256   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                        : promo == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                        : promo == 64  ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B
+                                                       : CU_TENSOR_MAP_L2_PROMOTION_NONE;
     const CUresult r = enc(&tp.map[c], dt, 2, p.out[c], dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, prom,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   if (ncomp == 1) tp.map[1] = tp.map[0];
@@ -371,6 +386,71 @@ KernelEntry phase_entry() {
     e.selfcheck = [] { return check_shape<S, false>("phase row"); };
     e.fn = (const void*)&fwt_phase_row_kernel<S>;
   }
+  return e;
+}
+
+template <class S, int KIND, int CL>
+cudaError_t launch_cluster(const PassParams& p, long long tiles, int ncomp, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)tiles, (unsigned)ncomp, 1);
+  cfg.blockDim = dim3(S::NT, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)4 << S::TB;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1u << CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fwt_cluster_kernel<S, KIND, CL>, p);
+}
+template <class S, int KIND, int CL>
+cudaError_t setup_cluster() {
+  cudaError_t err = cudaFuncSetAttribute(fwt_cluster_kernel<S, KIND, CL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)((size_t)4 << S::TB));
+  if (err == cudaSuccess && CL > 3)
+    err = cudaFuncSetAttribute(fwt_cluster_kernel<S, KIND, CL>,
+                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return err;
+}
+// Clusters of 2^CL CTAs that can be resident at once (0: the shape cannot run).
+template <class S, int KIND, int CL>
+int cluster_capacity() {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1u << CL, 1, 1);
+  cfg.blockDim = dim3(S::NT, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)4 << S::TB;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1u << CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fwt_cluster_kernel<S, KIND, CL>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+// One-pass transform of 2^(TB + CL)-element vectors on clusters of 2^CL CTAs
+// (fp32 / int32).  K = TB + CL is the vector's n.
+template <int DT, int KIND, int TB, int CL>
+KernelEntry cluster_entry() {
+  constexpr int EL = choose_el(TB, 2);
+  using S = Shape<TB, 0, TB, 2, TB - EL>;
+  KernelEntry e;
+  e.dtype = DT; e.kind = KIND_CLUSTER; e.K = TB + CL; e.TB = TB; e.TS = CL; e.col_bytes = 0;
+  e.tma = 0; e.threads = S::NT; e.smem = (size_t)4 << TB;
+  e.launch = &launch_cluster<S, KIND, CL>;
+  e.setup = &setup_cluster<S, KIND, CL>;
+  e.selfcheck = [] { return check_shape<S, false>("cluster slice"); };
+  e.fn = (const void*)&fwt_cluster_kernel<S, KIND, CL>;
+  e.capacity = &cluster_capacity<S, KIND, CL>;
   return e;
 }
 
