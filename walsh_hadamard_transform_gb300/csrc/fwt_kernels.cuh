@@ -58,25 +58,30 @@ struct PassParams {
 
 // ---- arithmetic policies ----------------------------------------------------------
 struct ArithF32 {
+  static constexpr bool kRadix4 = false;
   __device__ static float add(float a, float b) { return a + b; }
   __device__ static float sub(float a, float b) { return a - b; }
 };
-struct ArithU32 {  // two's complement wrap, bit-exact for int32 data
-  __device__ static uint32_t add(uint32_t a, uint32_t b) { return a + b; }
-  __device__ static uint32_t sub(uint32_t a, uint32_t b) { return a - b; }
-};
 struct ArithF64 {
+  static constexpr bool kRadix4 = false;
   __device__ static double add(double a, double b) { return a + b; }
   __device__ static double sub(double a, double b) { return a - b; }
 };
-struct ArithI64 {  // magnitudes stay below 2^62 by construction; no wrap occurs
-  __device__ static long long add(long long a, long long b) {
-    return (long long)((unsigned long long)a + (unsigned long long)b);
-  }
-  __device__ static long long sub(long long a, long long b) {
-    return (long long)((unsigned long long)a - (unsigned long long)b);
-  }
+// Integer policies: wrap-around arithmetic in unsigned types, with the three-operand
+// forms used by the two-stage butterflies.
+template <typename U, typename W>
+struct ArithInt {
+  static constexpr bool kRadix4 = true;
+  __device__ static U add(U a, U b) { return (U)((W)a + (W)b); }
+  __device__ static U sub(U a, U b) { return (U)((W)a - (W)b); }
+  __device__ static U add3(U a, U b, U c) { return (U)((W)a + (W)b + (W)c); }
+  __device__ static U add_sub(U a, U b, U c) { return (U)((W)a + (W)b - (W)c); }
+  __device__ static U sub2(U a, U b, U c) { return (U)((W)a - (W)b - (W)c); }
+  __device__ static U sub_add(U a, U b, U c) { return (U)((W)a - (W)b + (W)c); }
 };
+using ArithU32 = ArithInt<uint32_t, uint32_t>;  // two's complement wrap, bit-exact for int32
+// fixed point: magnitudes stay below 2^62 by construction; no wrap occurs
+using ArithI64 = ArithInt<long long, unsigned long long>;
 
 // ---- global memory access -------------------------------------------------------
 // Every load and store carries an L2 eviction-priority policy chosen per pass: the
@@ -316,7 +321,8 @@ __device__ __forceinline__ uint32_t abs_hi(long long bits) {
 
 // q = round(v * 2^(F + 1023 - emax)), ties away from zero, for |v| < 2^(emax - 1022):
 // |q| <= 2^(F+1).  Integer bit arithmetic only.
-// RIGHT: F <= 52, so every element shifts right (the common case, branch-free).
+// RIGHT: F <= 51, so every element shifts right by at least one bit (the common
+// case, branch-free, rounding folded into the shift).
 template <bool RIGHT>
 __device__ __forceinline__ long long to_fixed(long long bits, int emax, int F) {
   const unsigned long long b = (unsigned long long)bits;
@@ -326,9 +332,9 @@ __device__ __forceinline__ long long to_fixed(long long bits, int emax, int F) {
   // v = m * 2^(max(e,1) - 1075), so q = m * 2^(max(e,1) - emax + F - 52)
   const int sh = max(e, 1) - emax + F - 52;
   unsigned long long mag;
-  if constexpr (RIGHT) {  // sh <= F - 52 <= 0: always a rounding right shift
-    const int rs = min(-sh, 63);
-    mag = (((m << 1) >> rs) + 1ull) >> 1;
+  if constexpr (RIGHT) {  // sh <= F - 52 <= -1: shift by rs - 1 >= 0, add the half, halve
+    const int rs1 = min(-sh, 64) - 1;
+    mag = ((m >> rs1) + 1ull) >> 1;
   } else {  // either way, without a divergent branch: (sh >= 0: rs = 0, exact)
     const int rs = min(max(-sh, 0), 63);
     mag = ((((m << 1) >> rs) + 1ull) >> 1) << max(sh, 0);
@@ -389,7 +395,10 @@ __device__ __forceinline__ long long from_fixed_cvt(long long q, long long e0_fi
     q = (long long)((a ^ neg) - neg);
   }
   const long long b = __double_as_longlong(__ll2double_rn(q));
-  return q == 0 ? 0ll : b + e0_field;
+  // the exponent field sits in the high word, which is zero exactly when q == 0
+  const uint32_t hi = (uint32_t)((unsigned long long)b >> 32);
+  const uint32_t hi_scaled = hi == 0u ? 0u : hi + (uint32_t)((unsigned long long)e0_field >> 32);
+  return (long long)(((unsigned long long)hi_scaled << 32) | (uint32_t)b);
 }
 
 template <class S, class Mover, class Bits>
@@ -423,7 +432,7 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
   }
   const int emax = max((int)(key >> 20), 1);  // zeros and subnormals scale as exponent 1
   const int F = 61 - bits.tk;  // headroom: |q| <= 2^(F+1) grows by 2^tk
-  if (F <= 52) {  // (uniform) every element shifts right: the common case
+  if (F <= 51) {  // (uniform) every element shifts right: the common case
 #pragma unroll
     for (int r = 0; r < S::NE; ++r) x[r] = to_fixed<true>(x[r], emax, F);
   } else {

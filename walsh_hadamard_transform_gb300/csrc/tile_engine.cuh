@@ -147,20 +147,50 @@ struct Shape {
 // In-register butterflies over the register bits in `mask`: pairs (r, r | 2^h) with
 // bit h of r clear become (a + b, a - b).  A compile-time mask folds the tests
 // away; a run-time mask is uniform over the CTA, so its tests never diverge.
+//
+// Integer arithmetic (A::kRadix4) takes two stages at once where the mask allows:
+// a quadruple (a, b, c, d) = x[r], x[r+2^h], x[r+2^(h+1)], x[r+3*2^h] becomes
+// (a+b+c+d, a-b+c-d, a+b-c-d, a-b-c+d), six three-operand sums instead of eight
+// two-operand ones.  Integer sums are exact (or wrap identically), so grouping the
+// stages changes no bit of the result.
+template <class A, typename U>
+__device__ __forceinline__ void radix2(U& a, U& b) {
+  const U s = A::add(a, b), d = A::sub(a, b);
+  a = s;
+  b = d;
+}
+template <class A, typename U>
+__device__ __forceinline__ void radix4(U& a, U& b, U& c, U& d) {
+  const U s = A::add(a, b), t = A::sub(a, b);
+  const U y0 = A::add3(s, c, d);     // + + + +
+  const U y1 = A::add_sub(t, c, d);  // + - + -
+  const U y2 = A::sub2(s, c, d);     // + + - -
+  const U y3 = A::sub_add(t, c, d);  // + - - +
+  a = y0;
+  b = y1;
+  c = y2;
+  d = y3;
+}
 template <class A, int NE, typename U>
 __device__ __forceinline__ void butterflies(U (&x)[NE], uint32_t mask) {
+  constexpr int LOG = ilog2c(NE);
 #pragma unroll
-  for (int h = 0; h < ilog2c(NE); ++h) {
-    if ((mask >> h) & 1u) {
+  for (int h = 0; h < LOG; ++h) {
+    const bool here = (mask >> h) & 1u;
+    if constexpr (A::kRadix4) {
+      if (h + 1 < LOG && here && ((mask >> (h + 1)) & 1u)) {
 #pragma unroll
-      for (int r = 0; r < NE; ++r) {
-        if (!((r >> h) & 1)) {
-          const U a = x[r];
-          const U b = x[r | (1 << h)];
-          x[r] = A::add(a, b);
-          x[r | (1 << h)] = A::sub(a, b);
-        }
+        for (int r = 0; r < NE; ++r)
+          if (!((r >> h) & 3))
+            radix4<A>(x[r], x[r | (1 << h)], x[r | (2 << h)], x[r | (3 << h)]);
+        mask &= ~(2u << h);  // stage h + 1 is done
+        continue;
       }
+    }
+    if (here) {
+#pragma unroll
+      for (int r = 0; r < NE; ++r)
+        if (!((r >> h) & 1)) radix2<A>(x[r], x[r | (1 << h)]);
     }
   }
 }
