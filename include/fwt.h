@@ -16,9 +16,10 @@
  * Layout: batch-major and contiguous.  Vector b of each array occupies elements
  * [b * 2^n, (b + 1) * 2^n).  Each array holds batch * 2^n elements.
  *
- * Memory and ownership: every pointer is a DEVICE pointer owned by the caller.
- * The library allocates nothing, copies nothing to the host and never
- * synchronises: the work is enqueued on `stream` (NULL = the legacy default
+ * Memory and ownership: every pointer is a DEVICE pointer owned by the caller
+ * (the fwt_host_* entry points alone take host arrays and a device workspace).
+ * The library allocates no memory and never synchronises with the host: the
+ * work is enqueued on `stream` (NULL = the legacy default
  * stream of the current device) and the call returns at once.  Results are
  * valid after the caller synchronises with `stream`.  Pointers must be 16-byte
  * aligned (every cudaMalloc / PyTorch allocation is).
@@ -40,6 +41,7 @@
 #ifndef FWT_GB300_H
 #define FWT_GB300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -127,6 +129,52 @@ int fwt_phase_c32(const float* re_in, const float* im_in, const float* theta,
                   int64_t theta_stride, float* re_out, float* im_out, int n, int64_t batch,
                   int normalize, fwt_stream_t stream);
 
+/*
+ * Host-buffer transform: the same operation as fwt_batched_* on arrays in HOST
+ * memory, copied to the device, transformed and copied back.  (The pages describe
+ * the on-device transform only; this is the end-to-end form of it.)
+ *
+ * re_in, im_in, re_out, im_out: HOST pointers, layout as above (im_in == im_out
+ * == NULL allowed for int32 only).  Page-locked (pinned) host memory lets the
+ * copies run asynchronously and overlap; pageable memory works, with copies that
+ * serialise.  Each output may coincide exactly with its own input; any other
+ * overlap is rejected.
+ *
+ * workspace: DEVICE memory of workspace_bytes bytes, owned by the caller, 16-byte
+ * aligned; the library allocates nothing.  The batch is cut into chunks of whole
+ * vectors and the workspace holds up to three chunks at a time: the host-to-device
+ * copy of one chunk, the in-place transform of the previous one (on `stream`) and
+ * the device-to-host copy of the one before run concurrently, the copies on two
+ * streams the library creates once per device.  fwt_host_workspace_bytes() gives
+ * the size that lets the pipeline run at full depth; a smaller workspace gives
+ * smaller chunks or fewer slots, and one too small for a single vector is
+ * FWT_ERR_INVALID_ARG.
+ *
+ * Asynchronous like the device entry points: the call returns once everything is
+ * enqueued, and the outputs are complete when `stream` has reached the point of
+ * the call (e.g. after cudaStreamSynchronize(stream)).  Work enqueued on `stream`
+ * before the call completes before any copy starts.  The host buffers and the
+ * workspace must stay untouched until then.  Calls are serialised per process
+ * while they enqueue.  Errors as for fwt_batched_*; after FWT_ERR_CUDA earlier
+ * chunks may have been enqueued and the outputs are undefined.
+ */
+int fwt_host_c32(const float* re_in, const float* im_in, float* re_out, float* im_out, int n,
+                 int64_t batch, int normalize, void* workspace, size_t workspace_bytes,
+                 fwt_stream_t stream);
+int fwt_host_c64(const double* re_in, const double* im_in, double* re_out, double* im_out, int n,
+                 int64_t batch, int normalize, void* workspace, size_t workspace_bytes,
+                 fwt_stream_t stream);
+int fwt_host_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, int32_t* im_out,
+                 int n, int64_t batch, int normalize, void* workspace, size_t workspace_bytes,
+                 fwt_stream_t stream);
+
+/*
+ * Workspace bytes for fwt_host_* at full pipeline depth: three chunks of about
+ * batch / 16 vectors (at least 32 MiB, at most the batch), both parts unless
+ * with_im == 0 (int32 only).  0 for invalid arguments.
+ */
+size_t fwt_host_workspace_bytes(int dtype, int n, int64_t batch, int with_im);
+
 /* Static text for a status code (never NULL). */
 const char* fwt_status_string(int status);
 
@@ -174,8 +222,10 @@ int fwt_get_column_bytes(int dtype);
  * How column passes move their strided tiles: mode 2 stages every tile through
  * shared memory with TMA (cp.async.bulk.tensor) copies, 0 uses 16-byte vector
  * loads and stores, 1 (default) uses TMA for column factors of 10 or more bits
- * (tiles of 1024+ rows) and vector loads below.  All modes give identical
- * results.  Affects default plans and plans set afterwards.  Returns FWT_OK or
+ * (tiles of 1024+ rows) and vector loads below.  Modes 1 and 2 also stage whole
+ * fp64 row tiles with untiled bulk copies (cp.async.bulk); mode 0 loads them with
+ * vector loads.  All modes give identical results.  Affects default plans and
+ * plans set afterwards.  Returns FWT_OK or
  * FWT_ERR_INVALID_ARG; fwt_get_tma returns the mode.
  */
 int fwt_set_tma(int mode);

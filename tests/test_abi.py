@@ -168,3 +168,42 @@ def test_cluster_setting(lib):
     with pytest.raises(fwt.FwtError):
         fwt.set_cluster(5)
     fwt.set_cluster(fwt.CLUSTER_AUTO)
+
+
+@pytest.mark.parametrize("fn", ["fwt_host_c32", "fwt_host_c64", "fwt_host_i32"])
+def test_host_entry_argument_errors_before_any_cuda_call(lib, fn):
+    f = getattr(fwt, fn)
+    norm = 0 if fn.endswith("i32") else 1
+    a, b, c, d, w = A, A + GiB, A + 2 * GiB, A + 3 * GiB, A + 4 * GiB
+    ws = 1 << 30
+    assert f(a, b, c, d, -1, 1, norm, w, ws, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, c, d, 31, 1, norm, w, ws, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, c, d, 4, -1, norm, w, ws, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(None, None, None, None, 4, 0, norm, None, 0, None) == fwt.FWT_OK  # empty batch
+    assert f(a, b, c, d, 4, 1, norm, None, ws, None) == fwt.FWT_ERR_INVALID_ARG  # no workspace
+    assert f(a, b, c, d, 4, 1, norm, w + 8, ws, None) == fwt.FWT_ERR_MISALIGNED
+    assert f(a, b, c, None, 4, 1, norm, w, ws, None) == fwt.FWT_ERR_INVALID_ARG
+    # outputs overlapping anything but their own input exactly
+    assert f(a, b, a + 16, d, 4, 1, norm, w, ws, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, c, c, 4, 1, norm, w, ws, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, b, d, 4, 1, norm, w, ws, None) == fwt.FWT_ERR_INVALID_ARG
+    # a workspace too small for one vector (both parts)
+    esz = 8 if fn.endswith("c64") else 4
+    assert f(a, b, c, d, 10, 2, norm, w, 2 * esz * 1024 - 16, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, c, d, 30, 1 << 40, norm, w, ws, None) == fwt.FWT_ERR_INVALID_ARG
+    if fn.endswith("i32"):
+        assert f(a, None, c, None, 4, 1, 1, w, ws, None) == fwt.FWT_ERR_UNSUPPORTED
+    else:
+        assert f(a, None, c, None, 4, 1, norm, w, ws, None) == fwt.FWT_ERR_INVALID_ARG
+
+
+def test_host_workspace_size(lib):
+    ws = fwt.fwt_host_workspace_bytes
+    # n = 24 batch 16 fp64: chunks of one vector (2 parts x 128 MiB), three slots
+    assert ws(fwt.FWT_C64, 24, 16) == 3 * 2 * (8 << 24)
+    # small vectors: chunks of at least 32 MiB, never more than the batch
+    assert ws(fwt.FWT_C32, 10, 64) == 2 * 64 * 4096  # the whole batch is one chunk
+    # many vectors: chunks of batch / 16 vectors (here above the 32 MiB floor)
+    assert ws(fwt.FWT_I32, 12, 1 << 16, with_im=False) == 3 * 4096 * (4 << 12)
+    assert ws(fwt.FWT_I32, 12, 1 << 14, with_im=False) == 3 * 2048 * (4 << 12)
+    assert ws(fwt.FWT_C32, 4, 0) == 0 and ws(fwt.FWT_C32, 31, 1) == 0 and ws(7, 4, 1) == 0

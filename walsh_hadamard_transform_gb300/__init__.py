@@ -60,6 +60,12 @@ def library() -> ctypes.CDLL:
             f.restype = ci
         lib.fwt_phase_c32.argtypes = [vp, vp, vp, i64, vp, vp, ci, i64, ci, vp]
         lib.fwt_phase_c32.restype = ci
+        for name in ("fwt_host_c32", "fwt_host_c64", "fwt_host_i32"):
+            f = getattr(lib, name)
+            f.argtypes = [vp, vp, vp, vp, ci, i64, ci, vp, ctypes.c_size_t, vp]
+            f.restype = ci
+        lib.fwt_host_workspace_bytes.argtypes = [ci, ci, i64, ci]
+        lib.fwt_host_workspace_bytes.restype = ctypes.c_size_t
         lib.fwt_status_string.argtypes = [ci]
         lib.fwt_status_string.restype = ctypes.c_char_p
         lib.fwt_last_cuda_error.argtypes = []
@@ -135,6 +141,28 @@ def fwt_phase_c32(re_in, im_in, theta, theta_stride, re_out, im_out, n, batch, n
                   stream) -> int:
     return library().fwt_phase_c32(re_in, im_in, theta, theta_stride, re_out, im_out, n, batch,
                                    int(normalize), stream)
+
+
+def fwt_host_c32(re_in, im_in, re_out, im_out, n, batch, normalize, workspace, workspace_bytes,
+                 stream) -> int:
+    return library().fwt_host_c32(re_in, im_in, re_out, im_out, n, batch, int(normalize),
+                                  workspace, workspace_bytes, stream)
+
+
+def fwt_host_c64(re_in, im_in, re_out, im_out, n, batch, normalize, workspace, workspace_bytes,
+                 stream) -> int:
+    return library().fwt_host_c64(re_in, im_in, re_out, im_out, n, batch, int(normalize),
+                                  workspace, workspace_bytes, stream)
+
+
+def fwt_host_i32(re_in, im_in, re_out, im_out, n, batch, normalize, workspace, workspace_bytes,
+                 stream) -> int:
+    return library().fwt_host_i32(re_in, im_in, re_out, im_out, n, batch, int(normalize),
+                                  workspace, workspace_bytes, stream)
+
+
+def fwt_host_workspace_bytes(dtype, n, batch, with_im=True) -> int:
+    return int(library().fwt_host_workspace_bytes(int(dtype), int(n), int(batch), int(bool(with_im))))
 
 
 def phase_transform(re, im, theta, out_re=None, out_im=None, normalize: bool = True, stream=None):
@@ -309,6 +337,7 @@ class PassTrace:
 
 _ENTRY = {"c32": fwt_batched_c32, "c64": fwt_batched_c64, "i32": fwt_batched_i32}
 _BITS_ENTRY = {"c32": fwt_bits_c32, "c64": fwt_bits_c64, "i32": fwt_bits_i32}
+_HOST_ENTRY = {"c32": fwt_host_c32, "c64": fwt_host_c64, "i32": fwt_host_i32}
 
 
 def _dtype_key(t) -> str:
@@ -369,29 +398,63 @@ def transform(re, im=None, out_re=None, out_im=None, normalize: bool = True, str
     return out_re, out_im
 
 
-def transform_host(re, im=None, normalize: bool = True, device="cuda", stream=None,
-                   work=None):
-    """End-to-end transform of HOST tensors: copy in, transform on the GPU, copy out.
+def transform_host(re, im=None, out_re=None, out_im=None, normalize: bool = True, device="cuda",
+                   stream=None, workspace=None, synchronize: bool = True):
+    """End-to-end transform of HOST tensors through ``fwt_host_*``: the batch is
+    copied to ``device`` in chunks, transformed and copied back, the three stages of
+    successive chunks overlapping.
 
-    ``re`` / ``im`` are CPU tensors (pinned memory gives asynchronous copies).
-    ``work`` may hold preallocated device tensors (re_dev, im_dev) to reuse.
-    Returns host tensors (the result is complete when this returns).
+    ``re`` / ``im`` are contiguous CPU tensors of shape (batch, 2^n); page-locked
+    (pinned) memory lets the copies overlap.  Outputs are new host tensors (pinned
+    when the input is) unless ``out_re`` / ``out_im`` are given (they may be the
+    inputs).  ``workspace`` is a CUDA tensor of at least
+    ``fwt_host_workspace_bytes(...)`` bytes for full overlap (allocated here when
+    None).  With ``synchronize`` the call returns once the outputs are complete;
+    otherwise they are complete when ``stream`` reaches the call.  Returns
+    (out_re, out_im).
     """
     import torch
 
-    if work is None:
-        work = (torch.empty(re.shape, dtype=re.dtype, device=device),
-                None if im is None else torch.empty(im.shape, dtype=im.dtype, device=device))
-    dre, dim_ = work
-    dre.copy_(re, non_blocking=True)
-    if im is not None:
-        dim_.copy_(im, non_blocking=True)
-    transform(dre, dim_, dre, dim_, normalize=normalize, stream=stream)
-    hre = torch.empty(re.shape, dtype=re.dtype, pin_memory=re.is_pinned())
-    hre.copy_(dre, non_blocking=True)
-    him = None
-    if im is not None:
-        him = torch.empty(im.shape, dtype=im.dtype, pin_memory=im.is_pinned())
-        him.copy_(dim_, non_blocking=True)
-    torch.cuda.current_stream(dre.device).synchronize()
-    return hre, him
+    key = _dtype_key(re)
+    if re.is_cuda or (im is not None and im.is_cuda):
+        raise ValueError("transform_host() takes host tensors; use transform() for CUDA tensors")
+    if re.dim() != 2:
+        raise ValueError("expected a (batch, 2^n) tensor")
+    batch, N = re.shape
+    n = int(N).bit_length() - 1
+    if N < 1 or (1 << n) != N:
+        raise ValueError(f"row length {N} is not a power of two")
+    if out_re is None:
+        out_re = torch.empty(re.shape, dtype=re.dtype, pin_memory=re.is_pinned())
+    if im is not None and out_im is None:
+        out_im = torch.empty(im.shape, dtype=im.dtype, pin_memory=im.is_pinned())
+    for t in (re, im, out_re, out_im):
+        if t is None:
+            continue
+        if t.dtype != re.dtype or t.shape != re.shape or t.is_cuda:
+            raise ValueError("re, im and outputs must be host tensors of one dtype and shape")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    device = torch.device(device)
+    dt = DTYPES[key]
+    if workspace is None:
+        nbytes = fwt_host_workspace_bytes(dt, n, max(batch, 1), im is not None)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(workspace.device):
+        st = _HOST_ENTRY[key](re.data_ptr(), im.data_ptr() if im is not None else None,
+                              out_re.data_ptr(), out_im.data_ptr() if out_im is not None else None,
+                              n, batch, normalize, workspace.data_ptr(), ws_bytes, handle)
+    if st != FWT_OK:
+        raise FwtError(st, f"fwt_host_{key}(n={n}, batch={batch}, workspace={ws_bytes} B)")
+    if synchronize:
+        if hasattr(stream, "synchronize"):
+            stream.synchronize()
+        else:
+            torch.cuda.synchronize(workspace.device)
+    return out_re, out_im

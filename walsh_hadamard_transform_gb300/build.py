@@ -1,6 +1,6 @@
 """Build the CUDA library ``libfwt_gb300.so`` in-tree with nvcc (sm_103a only).
 
-Seven translation units are compiled in parallel and linked into one shared
+Eight translation units are compiled in parallel and linked into one shared
 library next to this file; objects go to ``_build/`` at the repository root.
 """
 from __future__ import annotations
@@ -18,8 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(ROOT, "_build")
 LIBRARY = os.path.join(PKG, "libfwt_gb300.so")
-SOURCES = ["fwt_api.cu", "rows_c32.cu", "rows_c64.cu", "rows_i32.cu", "cols_c32.cu",
-           "cols_c64.cu", "cols_i32.cu"]
+SOURCES = ["fwt_api.cu", "host_pipeline.cu", "rows_c32.cu", "rows_c64.cu", "rows_i32.cu",
+           "cols_c32.cu", "cols_c64.cu", "cols_i32.cu"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

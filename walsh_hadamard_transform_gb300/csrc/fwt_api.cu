@@ -457,6 +457,7 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
         p.do_scale = (normalize && last) ? 1 : 0;
         p.ld_policy = 1;                             // read once
         p.st_policy = last ? 1 : (chunked ? 2 : 0);  // keep intermediates for the next pass
+        p.bulk = g_use_tma != 0 ? 1 : 0;             // bulk-copied fp64 row tiles
         const bool traced = g_trace_count + 2 <= g_trace_capacity;
         if (traced) {
           err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count], stream);
@@ -566,6 +567,7 @@ int run_phase(const float* re_in, const float* im_in, const float* theta, int64_
 }  // namespace
 
 int tma_l2_promotion() { return g_tma_promotion.load(); }
+void set_last_cuda_error(int err) { g_last_cuda_error = err; }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   std::call_once(g_encoder_once, [] {

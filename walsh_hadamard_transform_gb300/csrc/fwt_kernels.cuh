@@ -54,6 +54,7 @@ struct PassParams {
   const float* theta;    // phase pass: angles, theta[b * theta_stride + i]
   long long theta_stride;
   int n;                 // phase pass: log2 of the vector length
+  int bulk;              // row tiles: stage whole tiles with bulk copies where eligible
 };
 
 // ---- arithmetic policies ----------------------------------------------------------
@@ -68,10 +69,12 @@ struct ArithF64 {
   __device__ static double sub(double a, double b) { return a - b; }
 };
 // Integer policies: wrap-around arithmetic in unsigned types, with the three-operand
-// forms used by the two-stage butterflies.
-template <typename U, typename W>
+// forms used by the two-stage butterflies.  The int32 passes are bound by HBM, not by
+// issue, and measured no faster at radix 4 (one short column pass slower), so only
+// the 64-bit fixed-point arithmetic takes it.
+template <typename U, typename W, bool RADIX4>
 struct ArithInt {
-  static constexpr bool kRadix4 = true;
+  static constexpr bool kRadix4 = RADIX4;
   __device__ static U add(U a, U b) { return (U)((W)a + (W)b); }
   __device__ static U sub(U a, U b) { return (U)((W)a - (W)b); }
   __device__ static U add3(U a, U b, U c) { return (U)((W)a + (W)b + (W)c); }
@@ -79,9 +82,9 @@ struct ArithInt {
   __device__ static U sub2(U a, U b, U c) { return (U)((W)a - (W)b - (W)c); }
   __device__ static U sub_add(U a, U b, U c) { return (U)((W)a - (W)b + (W)c); }
 };
-using ArithU32 = ArithInt<uint32_t, uint32_t>;  // two's complement wrap, bit-exact for int32
+using ArithU32 = ArithInt<uint32_t, uint32_t, false>;  // two's complement wrap, bit-exact
 // fixed point: magnitudes stay below 2^62 by construction; no wrap occurs
-using ArithI64 = ArithInt<long long, unsigned long long>;
+using ArithI64 = ArithInt<long long, unsigned long long, true>;
 
 // ---- global memory access -------------------------------------------------------
 // Every load and store carries an L2 eviction-priority policy chosen per pass: the
@@ -213,6 +216,18 @@ struct TmaPassParams {
   PassParams p;
 };
 
+// Waits (bounded) for a staged tile on its mbarrier, as a CTA-wide decision.  On
+// give-up every thread learns it, and the copies still in flight get one more
+// bounded wait so the CTA does not leave while they may still write its shared
+// memory.
+__device__ __forceinline__ bool wait_tile(uint64_t* bar) {
+  const bool ok = mbar_wait_bounded(bar, 0);
+  if (!__syncthreads_or(!ok)) return true;
+  if (threadIdx.x == 0) mbar_wait_bounded(bar, 0);
+  __syncthreads();
+  return false;
+}
+
 // TMA: the column tile arrives in shared memory in natural order; threads pick up
 // layout L1 there, and write layout L3 back there for a TMA store.
 template <class S>
@@ -245,8 +260,7 @@ struct TmaMover {
       for (int i = 0; i < NBOX; ++i)
         tma_load_2d(smem + (size_t)i * BOX_ELEMS * sizeof(U), map, col0, row0 + i * BOXR, bar, pol);
     }
-    const bool ok = mbar_wait_bounded(bar, 0);
-    if (__syncthreads_or(!ok)) return false;  // the whole tile is skipped
+    if (!wait_tile(bar)) return false;  // the whole tile is skipped
     const U* sm = reinterpret_cast<const U*>(smem);
 #pragma unroll
     for (int j = 0; j < S::NV; ++j) get_vec<U, S::VEC>(sm + S::idx1(threadIdx.x, j * S::VEC), x, j);
@@ -266,6 +280,63 @@ struct TmaMover {
 #pragma unroll
       for (int i = 0; i < NBOX; ++i)
         tma_store_2d(map, col0, row0 + i * BOXR, smem + (size_t)i * BOX_ELEMS * sizeof(U), pol);
+      tma_store_commit_and_wait();
+    }
+  }
+};
+
+// Bulk: a contiguous row tile (2^TB elements, never ragged) arrives in shared
+// memory in natural order through untiled bulk copies (16 KiB each) that complete
+// on one mbarrier; threads pick up layout L1 there and write layout L3 back for
+// bulk stores.  The loads bypass L1 and the registers, like the TMA column tiles.
+template <class S>
+struct BulkMover {
+  const char* src;
+  char* dst;
+  unsigned char* smem;
+  uint64_t* bar;
+  __device__ BulkMover(const PassParams& p, unsigned char* smem_raw, uint64_t* barrier) {
+    const bool im = blockIdx.y != 0;
+    src = static_cast<const char*>(im ? p.in[1] : p.in[0]);
+    dst = static_cast<char*>(im ? p.out[1] : p.out[0]);
+    smem = smem_raw;
+    bar = barrier;
+    if (threadIdx.x == 0) mbar_init(bar, 1);
+    __syncthreads();
+  }
+  template <typename U>
+  __device__ __forceinline__ bool load(U (&x)[S::NE], int policy) {
+    constexpr uint32_t BYTES = (uint32_t)sizeof(U) << S::TB;
+    constexpr uint32_t CH = BYTES < 16384u ? BYTES : 16384u;
+    if (threadIdx.x == 0) {
+      const unsigned long long pol = l2_policy(policy);
+      const char* g = src + (size_t)blockIdx.x * BYTES;
+      mbar_arrive_expect_tx(bar, BYTES);
+#pragma unroll
+      for (uint32_t o = 0; o < BYTES; o += CH) bulk_load(smem + o, g + o, CH, bar, pol);
+    }
+    if (!wait_tile(bar)) return false;  // the whole tile is skipped
+    const U* sm = reinterpret_cast<const U*>(smem);
+#pragma unroll
+    for (int j = 0; j < S::NV; ++j) get_vec<U, S::VEC>(sm + S::idx1(threadIdx.x, j * S::VEC), x, j);
+    __syncthreads();  // the tile engine reuses the buffer
+    return true;
+  }
+  template <typename U>
+  __device__ __forceinline__ void store(const U (&x)[S::NE], int policy) {
+    constexpr uint32_t BYTES = (uint32_t)sizeof(U) << S::TB;
+    constexpr uint32_t CH = BYTES < 16384u ? BYTES : 16384u;
+    U* sm = reinterpret_cast<U*>(smem);
+    __syncthreads();  // the engine's last reads of the buffer are done
+#pragma unroll
+    for (int j = 0; j < S::NV; ++j) put_vec<U, S::VEC>(sm + S::idx3(threadIdx.x, j * S::VEC), x, j);
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const unsigned long long pol = l2_policy(policy);
+      char* g = dst + (size_t)blockIdx.x * BYTES;
+#pragma unroll
+      for (uint32_t o = 0; o < BYTES; o += CH) bulk_store(g + o, smem + o, CH, pol);
       tma_store_commit_and_wait();
     }
   }
@@ -481,6 +552,18 @@ __global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1)) fwt_ti
   tile_body<S, KIND>(p, smem_raw, mv, StaticBits<S>(p));
 }
 
+// Row pass with bulk-copied tiles (fp64 fixed point: 3 CTAs an SM, as the TMA column
+// pass; whole tiles only).
+template <class S, int KIND>
+__global__ void __launch_bounds__(S::NT, KIND == 1 ? (S::NT < 768 ? 768 / S::NT : 1)
+                                                   : (S::NT < 512 ? 512 / S::NT : 1))
+    fwt_row_bulk_kernel(const PassParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bar;
+  BulkMover<S> mv(p, smem_raw, &bar);
+  tile_body<S, KIND>(p, smem_raw, mv, StaticBits<S>(p));
+}
+
 // Contiguous tiles of 2^TB elements whose transformed bits [bits_lo, bits_lo +
 // bits_k) are chosen at run time: a transform on a sub-range of the index bits
 // that lies within the low TB bits (several vectors per tile when 2^n < 2^TB).
@@ -492,9 +575,13 @@ __global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
   tile_body<S, KIND>(p, smem_raw, mv, RuntimeBits<S>(p));
 }
 
-// Column pass with TMA-staged tiles.
+// Column pass with TMA-staged tiles.  The fp64 fixed-point variant is issue-bound
+// and its loads do not go through L1, so it trades registers (80 a thread, a few
+// spilled) for a third resident CTA per SM: 24 warps instead of 16 hide more of the
+// TMA and integer latencies (about 20% faster at 2^13-element tiles).
 template <class S, int KIND>
-__global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
+__global__ void __launch_bounds__(S::NT, KIND == 1 ? (S::NT < 768 ? 768 / S::NT : 1)
+                                                   : (S::NT < 512 ? 512 / S::NT : 1))
     fwt_col_tma_kernel(const __grid_constant__ TmaPassParams tp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bar;

@@ -1,0 +1,199 @@
+// Host-buffer entry points: copy in, transform, copy out, as a three-stage
+// pipeline over chunks of whole vectors.
+//
+// The batch is cut into chunks of c vectors.  A caller-provided device workspace
+// holds up to three chunks (slots).  Chunk k is copied host -> device on the
+// library's copy-in stream, transformed in place on the caller's stream, and
+// copied device -> host on the copy-out stream; events order the three stages of
+// one chunk and keep a slot from being refilled before its previous chunk has
+// left.  So the host -> device copy of chunk k+1, the transform of chunk k and the
+// device -> host copy of chunk k-1 run at the same time, and both directions of
+// the host link are busy at once.
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fwt.h"
+#include "registry.cuh"
+
+namespace fwt {
+namespace {
+
+constexpr int kSlots = 3;
+constexpr size_t kSlotAlign = 256;          // slot parts start on 256-byte boundaries
+constexpr size_t kTargetChunkBytes = 32ull << 20;  // smallest chunk worth a pipeline stage
+constexpr int64_t kTargetChunks = 16;
+
+struct DeviceStreams {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr;
+  cudaEvent_t loaded[kSlots] = {}, done[kSlots] = {}, drained[kSlots] = {};
+};
+
+std::mutex g_mu;
+std::vector<DeviceStreams> g_dev;
+
+cudaError_t streams_for_current_device(DeviceStreams*& ds) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if ((int)g_dev.size() <= dev) g_dev.resize(dev + 1);
+  ds = &g_dev[dev];
+  if (ds->ready) return cudaSuccess;
+  err = cudaStreamCreateWithFlags(&ds->in, cudaStreamNonBlocking);
+  if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&ds->out, cudaStreamNonBlocking);
+  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ds->start, cudaEventDisableTiming);
+  for (int s = 0; s < kSlots && err == cudaSuccess; ++s) {
+    err = cudaEventCreateWithFlags(&ds->loaded[s], cudaEventDisableTiming);
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ds->done[s], cudaEventDisableTiming);
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ds->drained[s], cudaEventDisableTiming);
+  }
+  if (err == cudaSuccess) ds->ready = true;
+  return err;
+}
+
+size_t align_up(size_t v) { return (v + kSlotAlign - 1) / kSlotAlign * kSlotAlign; }
+
+// Bytes of one slot holding c vectors of `parts` arrays.
+size_t slot_bytes(int esz, int n, int64_t c, int parts) {
+  return (size_t)parts * align_up((size_t)(c << n) * (size_t)esz);
+}
+
+// Vectors a chunk should hold: about batch / 16, at least 32 MiB, at most the batch.
+int64_t target_chunk(int esz, int n, int64_t batch, int parts) {
+  const size_t vec = (size_t)parts * ((size_t)1 << n) * (size_t)esz;
+  int64_t c = (batch + kTargetChunks - 1) / kTargetChunks;
+  c = std::max<int64_t>(c, (int64_t)((kTargetChunkBytes + vec - 1) / vec));
+  return std::max<int64_t>(1, std::min(c, batch));
+}
+
+int run_host(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out, int n,
+             int64_t batch, int normalize, void* workspace, size_t workspace_bytes,
+             cudaStream_t stream) {
+  if (n < 0 || n > 30 || batch < 0) return FWT_ERR_INVALID_ARG;
+  if (batch == 0) return FWT_OK;
+  const int esz = dtype == FWT_C64 ? 8 : 4;
+  if (batch > (INT64_MAX >> n) / esz) return FWT_ERR_INVALID_ARG;
+  if (!re_in || !re_out || !workspace) return FWT_ERR_INVALID_ARG;
+  const bool has_im = im_in || im_out;
+  if (has_im && (!im_in || !im_out)) return FWT_ERR_INVALID_ARG;
+  if (!has_im && dtype != FWT_I32) return FWT_ERR_INVALID_ARG;
+  if (dtype == FWT_I32 && normalize) return FWT_ERR_UNSUPPORTED;
+  if ((uintptr_t)workspace & 15u) return FWT_ERR_MISALIGNED;
+  const size_t bytes = (size_t)(batch << n) * (size_t)esz;
+  // host outputs may coincide exactly with their own input, and with nothing else
+  auto disjoint = [bytes](const void* a, const void* b) {
+    return (uintptr_t)a + bytes <= (uintptr_t)b || (uintptr_t)b + bytes <= (uintptr_t)a;
+  };
+  if (re_out != re_in && !disjoint(re_out, re_in)) return FWT_ERR_INVALID_ARG;
+  if (has_im) {
+    if (im_out != im_in && !disjoint(im_out, im_in)) return FWT_ERR_INVALID_ARG;
+    if (!disjoint(re_out, im_out) || !disjoint(re_out, im_in) || !disjoint(im_out, re_in))
+      return FWT_ERR_INVALID_ARG;
+  }
+  const int parts = has_im ? 2 : 1;
+  // chunk size and slot count from the workspace
+  int64_t c = target_chunk(esz, n, batch, parts);
+  while (c > 1 && slot_bytes(esz, n, c, parts) * kSlots > workspace_bytes) c = (c + 1) / 2;
+  const size_t sb = slot_bytes(esz, n, c, parts);
+  const int slots = (int)std::min<size_t>(kSlots, workspace_bytes / sb);
+  if (slots < 1) return FWT_ERR_INVALID_ARG;  // not even one vector fits
+  const size_t part_off = align_up((size_t)(c << n) * (size_t)esz);
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceStreams* ds = nullptr;
+  cudaError_t err = streams_for_current_device(ds);
+  auto fail = [&](cudaError_t e) {
+    set_last_cuda_error((int)e);
+    return FWT_ERR_CUDA;
+  };
+  if (err != cudaSuccess) return fail(err);
+  // nothing starts before the work the caller enqueued on `stream` so far
+  err = cudaEventRecord(ds->start, stream);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(ds->in, ds->start, 0);
+  if (err == cudaSuccess) err = cudaStreamWaitEvent(ds->out, ds->start, 0);
+  if (err != cudaSuccess) return fail(err);
+
+  const int64_t chunks = (batch + c - 1) / c;
+  for (int64_t k = 0; k < chunks; ++k) {
+    const int s = (int)(k % slots);
+    const int64_t v0 = k * c, nv = std::min(c, batch - v0);
+    const size_t off = (size_t)(v0 << n) * (size_t)esz, len = (size_t)(nv << n) * (size_t)esz;
+    char* d_re = (char*)workspace + (size_t)s * sb;
+    char* d_im = has_im ? d_re + part_off : nullptr;
+    // copy in, once the slot's previous chunk has been copied out
+    if (k >= slots) err = cudaStreamWaitEvent(ds->in, ds->drained[s], 0);
+    if (err == cudaSuccess)
+      err = cudaMemcpyAsync(d_re, (const char*)re_in + off, len, cudaMemcpyHostToDevice, ds->in);
+    if (err == cudaSuccess && has_im)
+      err = cudaMemcpyAsync(d_im, (const char*)im_in + off, len, cudaMemcpyHostToDevice, ds->in);
+    if (err == cudaSuccess) err = cudaEventRecord(ds->loaded[s], ds->in);
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(stream, ds->loaded[s], 0);
+    if (err != cudaSuccess) return fail(err);
+    // transform in place on the caller's stream
+    int st;
+    if (dtype == FWT_C32)
+      st = fwt_batched_c32((const float*)d_re, (const float*)d_im, (float*)d_re, (float*)d_im, n,
+                           nv, normalize, stream);
+    else if (dtype == FWT_C64)
+      st = fwt_batched_c64((const double*)d_re, (const double*)d_im, (double*)d_re,
+                           (double*)d_im, n, nv, normalize, stream);
+    else
+      st = fwt_batched_i32((const int32_t*)d_re, (const int32_t*)d_im, (int32_t*)d_re,
+                           (int32_t*)d_im, n, nv, 0, stream);
+    if (st != FWT_OK) return st;
+    err = cudaEventRecord(ds->done[s], stream);
+    // copy out
+    if (err == cudaSuccess) err = cudaStreamWaitEvent(ds->out, ds->done[s], 0);
+    if (err == cudaSuccess)
+      err = cudaMemcpyAsync((char*)re_out + off, d_re, len, cudaMemcpyDeviceToHost, ds->out);
+    if (err == cudaSuccess && has_im)
+      err = cudaMemcpyAsync((char*)im_out + off, d_im, len, cudaMemcpyDeviceToHost, ds->out);
+    if (err == cudaSuccess) err = cudaEventRecord(ds->drained[s], ds->out);
+    if (err != cudaSuccess) return fail(err);
+  }
+  // the caller's stream reaches this point only after the last copy out
+  err = cudaStreamWaitEvent(stream, ds->drained[(chunks - 1) % slots], 0);
+  return err == cudaSuccess ? FWT_OK : fail(err);
+}
+
+}  // namespace
+}  // namespace fwt
+
+extern "C" {
+
+size_t fwt_host_workspace_bytes(int dtype, int n, int64_t batch, int with_im) {
+  if (dtype < 0 || dtype > 2 || n < 0 || n > 30 || batch <= 0) return 0;
+  const int esz = dtype == FWT_C64 ? 8 : 4;
+  const int parts = (with_im || dtype != FWT_I32) ? 2 : 1;
+  const int64_t c = fwt::target_chunk(esz, n, batch, parts);
+  const int64_t chunks = (batch + c - 1) / c;
+  return fwt::slot_bytes(esz, n, c, parts) * (size_t)std::min<int64_t>(fwt::kSlots, chunks);
+}
+
+int fwt_host_c32(const float* re_in, const float* im_in, float* re_out, float* im_out, int n,
+                 int64_t batch, int normalize, void* workspace, size_t workspace_bytes,
+                 fwt_stream_t stream) {
+  return fwt::run_host(FWT_C32, re_in, im_in, re_out, im_out, n, batch, normalize, workspace,
+                       workspace_bytes, (cudaStream_t)stream);
+}
+
+int fwt_host_c64(const double* re_in, const double* im_in, double* re_out, double* im_out, int n,
+                 int64_t batch, int normalize, void* workspace, size_t workspace_bytes,
+                 fwt_stream_t stream) {
+  return fwt::run_host(FWT_C64, re_in, im_in, re_out, im_out, n, batch, normalize, workspace,
+                       workspace_bytes, (cudaStream_t)stream);
+}
+
+int fwt_host_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, int32_t* im_out,
+                 int n, int64_t batch, int normalize, void* workspace, size_t workspace_bytes,
+                 fwt_stream_t stream) {
+  return fwt::run_host(FWT_I32, re_in, im_in, re_out, im_out, n, batch, normalize, workspace,
+                       workspace_bytes, (cudaStream_t)stream);
+}
+
+}  // extern "C"
