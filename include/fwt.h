@@ -209,11 +209,14 @@ int fwt_set_plan(int n, int dtype, int nfactors, const int* bits);
 /*
  * Tuning: bytes of contiguous columns (16, 32, 64 or 128) that each tile of a
  * column pass reads from every row it touches.  Wider segments make longer DRAM
- * bursts; narrower ones shrink the tile so that more CTAs share an SM.  16-byte
- * tiles are always staged by TMA copies.
- * Affects default plans and plans set afterwards for `dtype`.  Returns FWT_OK or
- * FWT_ERR_INVALID_ARG; fwt_get_column_bytes returns the current width (-1 for an
- * invalid dtype).
+ * bursts; narrower ones shrink the tile so that more CTAs share an SM, or let a
+ * column factor grow.  16-byte tiles are always staged by TMA copies.  0 (the
+ * default) chooses per plan: 64 bytes (fp32/int32) or 32 (fp64), and the measured
+ * two-pass splits with narrower segments for large n (4-byte n = 26..28, fp64
+ * n = 26); a plan set with fwt_set_plan gets the first width whose tiles cover its
+ * factors.  Affects default plans and plans set afterwards for `dtype`.  Returns
+ * FWT_OK or FWT_ERR_INVALID_ARG; fwt_get_column_bytes returns the setting (0 =
+ * per plan, -1 for an invalid dtype).
  */
 int fwt_set_column_bytes(int dtype, int bytes);
 int fwt_get_column_bytes(int dtype);

@@ -92,6 +92,12 @@ def test_plans(lib):
             assert (len(f) == 1) == (n <= rmax) or (cluster_ok and len(f) == 1)
     assert fwt.plan_factors(24, "c32") == [14, 10]
     assert fwt.plan_factors(24, "c64") == [13, 11]
+    if fwt.column_bytes("c32") == 0 and fwt.column_bytes("c64") == 0:
+        # measured two-pass splits with narrower column segments for large n
+        assert fwt.plan_factors(27, "c32") == [15, 12]
+        assert fwt.plan_factors(28, "i32") == [15, 13]
+        assert fwt.plan_factors(26, "c64") == [13, 13]
+        assert len(fwt.plan_factors(29, "c32")) == 3
     assert lib.fwt_plan_passes(31, 0) == -1 and lib.fwt_plan_passes(10, 7) == -1
 
 
@@ -107,15 +113,32 @@ def test_plan_override_roundtrip(lib):
         fwt.set_plan(20, "c32", None)
         fwt.set_column_bytes("c32", width)
     assert fwt.plan_factors(20, "c32") == default
-    for bad in ([10, 9], [16, 4], [2, 18], [3, 7, 10], [10, 11], [10, 5, 5]):
-        with pytest.raises(fwt.FwtError):
-            fwt.set_plan(20, "c32", bad)
+    fwt.set_column_bytes("c32", 64)
+    try:
+        for bad in ([10, 9], [16, 4], [2, 18], [3, 7, 10], [10, 11], [10, 5, 5]):
+            with pytest.raises(fwt.FwtError):
+                fwt.set_plan(20, "c32", bad)
+    finally:
+        fwt.set_column_bytes("c32", width)
     assert fwt.plan_factors(20, "c32") == default
+    # with the width chosen per plan, a plan takes the first width that has tiles
+    # for all its factors: 5-bit column factors need 128-byte segments, a 3-bit row
+    # factor segments of at most 2^3 elements
+    if width == 0:
+        try:
+            for ok in ([10, 5, 5], [3, 7, 10]):
+                fwt.set_plan(20, "c32", ok)
+                assert fwt.plan_factors(20, "c32") == ok
+        finally:
+            fwt.set_plan(20, "c32", None)
+        for bad in ([10, 9], [16, 4], [2, 18], [10, 11], [3, 3, 14]):
+            with pytest.raises(fwt.FwtError):
+                fwt.set_plan(20, "c32", bad)
 
 
 def test_column_bytes_setting(lib):
     for dt in ("c32", "c64", "i32"):
-        assert fwt.column_bytes(dt) in (16, 32, 64, 128)
+        assert fwt.column_bytes(dt) in (0, 16, 32, 64, 128)
     with pytest.raises(fwt.FwtError):
         fwt.set_column_bytes("c32", 96)
     with pytest.raises(fwt.FwtError):

@@ -232,7 +232,8 @@ def set_plan(n: int, dtype: str, factors) -> None:
 
 
 def set_column_bytes(dtype: str, nbytes: int) -> None:
-    """Column-pass segment width (64 or 128 bytes) for later plans of ``dtype``."""
+    """Column-pass segment width (16, 32, 64 or 128 bytes; 0 = chosen per plan, the
+    default) for later plans of ``dtype``."""
     st = library().fwt_set_column_bytes(DTYPES[dtype], int(nbytes))
     if st != FWT_OK:
         raise FwtError(st, f"fwt_set_column_bytes({dtype}, {nbytes})")

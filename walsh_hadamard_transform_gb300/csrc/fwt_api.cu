@@ -77,7 +77,8 @@ int col_tma(const Plan& p, int K) {
 
 std::mutex g_plan_mu;
 Plan g_override[3][31];  // nf == 0: no override
-int g_col_bytes[3] = {64, 32, 64};  // default column segment width per dtype
+int g_col_bytes[3] = {0, 0, 0};  // column segment width per dtype; 0: chosen per plan
+int default_col_bytes(int dtype) { return dtype == FWT_C64 ? 32 : 64; }
 int g_use_tma = 1;                    // TMA-staged column passes: 0 never, 1 auto, 2 always
 int g_use_cluster = 1;                // one-pass cluster kernels: 0 never, 1 auto, 2 from n = 14
 
@@ -111,12 +112,38 @@ bool plan_valid(int n, int dtype, const Plan& p) {
   return sum == n;
 }
 
+// Two-pass splits measured faster than the general rule for large vectors (GB300,
+// default widths otherwise): narrower column segments let the column factor grow
+// so that n = 27, 28 (4-byte) need two passes instead of three, and fp64 n = 26
+// keeps its row factor at 13 bits (bulk-copied tiles).
+struct LargeSplit {
+  bool fp64;
+  int n, row, col, col_bytes;
+};
+constexpr LargeSplit kLargeSplits[] = {
+    {false, 26, 14, 12, 32}, {false, 27, 15, 12, 32}, {false, 28, 15, 13, 16},
+    {true, 26, 13, 13, 16},
+};
+
 Plan default_plan(int n, int dtype) {
   Plan p;
+  int width;
   {
     std::lock_guard<std::mutex> lk(g_plan_mu);
-    p.col_bytes = g_col_bytes[dtype];
+    width = g_col_bytes[dtype];
     p.tma = g_use_tma;
+  }
+  p.col_bytes = width ? width : default_col_bytes(dtype);
+  if (width == 0) {
+    for (const LargeSplit& ls : kLargeSplits) {
+      if (ls.fp64 != (dtype == FWT_C64) || ls.n != n) continue;
+      Plan q = p;
+      q.nf = 2;
+      q.bits[0] = ls.row;
+      q.bits[1] = ls.col;
+      q.col_bytes = ls.col_bytes;
+      if (plan_valid(n, dtype, q)) return q;
+    }
   }
   const int rmax = max_row_bits(dtype), cmin = min_col_bits(dtype, p.col_bytes),
             cmax = max_col_bits(dtype, p.col_bytes);
@@ -663,23 +690,33 @@ int fwt_set_plan(int n, int dtype, int nfactors, const int* bits) {
     return FWT_ERR_INVALID_ARG;
   fwt::Plan p;
   p.nf = nfactors;
+  int width;
   {
     std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
-    p.col_bytes = fwt::g_col_bytes[dtype];
+    width = fwt::g_col_bytes[dtype];
     p.tma = fwt::g_use_tma;
   }
   for (int f = 0; f < nfactors; ++f) {
     if (!bits) return FWT_ERR_INVALID_ARG;
     p.bits[f] = bits[f];
   }
-  if (nfactors > 0 && !fwt::plan_valid(n, dtype, p)) return FWT_ERR_UNSUPPORTED;
+  if (nfactors > 0) {
+    // the width set for the dtype, else the first width with tiles for every factor
+    bool ok = false;
+    for (int cb : {width ? width : fwt::default_col_bytes(dtype), 32, 16, 64, 128}) {
+      p.col_bytes = cb;
+      if ((ok = fwt::plan_valid(n, dtype, p)) || width) break;
+    }
+    if (!ok) return FWT_ERR_UNSUPPORTED;
+  }
   std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
   fwt::g_override[dtype][n] = p;
   return FWT_OK;
 }
 
 int fwt_set_column_bytes(int dtype, int bytes) {
-  if (dtype < 0 || dtype > 2 || (bytes != 16 && bytes != 32 && bytes != 64 && bytes != 128))
+  if (dtype < 0 || dtype > 2 ||
+      (bytes != 0 && bytes != 16 && bytes != 32 && bytes != 64 && bytes != 128))
     return FWT_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(fwt::g_plan_mu);
   fwt::g_col_bytes[dtype] = bytes;
