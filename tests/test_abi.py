@@ -96,7 +96,8 @@ def test_plans(lib):
         # measured two-pass splits with narrower column segments for large n
         assert fwt.plan_factors(27, "c32") == [15, 12]
         assert fwt.plan_factors(28, "i32") == [15, 13]
-        assert fwt.plan_factors(26, "c64") == [13, 13]
+        assert fwt.plan_factors(25, "c64") == [14, 11]
+        assert fwt.plan_factors(26, "c64") == [12, 6, 8]
         assert len(fwt.plan_factors(29, "c32")) == 3
     assert lib.fwt_plan_passes(31, 0) == -1 and lib.fwt_plan_passes(10, 7) == -1
 

@@ -112,17 +112,21 @@ bool plan_valid(int n, int dtype, const Plan& p) {
   return sum == n;
 }
 
-// Two-pass splits measured faster than the general rule for large vectors (GB300,
-// default widths otherwise): narrower column segments let the column factor grow
-// so that n = 27, 28 (4-byte) need two passes instead of three, and fp64 n = 26
-// keeps its row factor at 13 bits (bulk-copied tiles).
+// Splits measured faster than the general rule for large vectors (GB300, 2^28
+// elements a part).  4-byte types: narrower column segments let the column factor
+// grow, so n = 27, 28 need two passes instead of three.  fp64: tiles of 2^14
+// elements run one 512-thread CTA an SM and no faster than half the rate of the
+// 2^13-element tiles (three CTAs an SM), so from n = 26 three passes over tiles of
+// at most 2^13 elements (128-byte segments) beat two passes that need one.
 struct LargeSplit {
   bool fp64;
-  int n, row, col, col_bytes;
+  int n, nf, bits[3], col_bytes;
 };
 constexpr LargeSplit kLargeSplits[] = {
-    {false, 26, 14, 12, 32}, {false, 27, 15, 12, 32}, {false, 28, 15, 13, 16},
-    {true, 26, 13, 13, 16},
+    {false, 25, 2, {14, 11, 0}, 32},  {false, 26, 2, {14, 12, 0}, 32},
+    {false, 27, 2, {15, 12, 0}, 32},  {false, 28, 2, {15, 13, 0}, 16},
+    {true, 25, 2, {14, 11, 0}, 32},   {true, 26, 3, {12, 6, 8}, 128},
+    {true, 27, 3, {12, 7, 8}, 128},   {true, 28, 3, {12, 8, 8}, 128},
 };
 
 Plan default_plan(int n, int dtype) {
@@ -138,9 +142,8 @@ Plan default_plan(int n, int dtype) {
     for (const LargeSplit& ls : kLargeSplits) {
       if (ls.fp64 != (dtype == FWT_C64) || ls.n != n) continue;
       Plan q = p;
-      q.nf = 2;
-      q.bits[0] = ls.row;
-      q.bits[1] = ls.col;
+      q.nf = ls.nf;
+      for (int f = 0; f < 3; ++f) q.bits[f] = ls.bits[f];
       q.col_bytes = ls.col_bytes;
       if (plan_valid(n, dtype, q)) return q;
     }

@@ -575,13 +575,19 @@ __global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
   tile_body<S, KIND>(p, smem_raw, mv, RuntimeBits<S>(p));
 }
 
-// Column pass with TMA-staged tiles.  The fp64 fixed-point variant is issue-bound
-// and its loads do not go through L1, so it trades registers (80 a thread, a few
-// spilled) for a third resident CTA per SM: 24 warps instead of 16 hide more of the
-// TMA and integer latencies (about 20% faster at 2^13-element tiles).
+// Column pass with TMA-staged tiles.  The loads do not go through L1, so the kernel
+// can trade registers (80 a thread, a few spilled to L1) for a third resident CTA
+// per SM: 24 warps instead of 16 hide more of the TMA and integer latencies.  Taken
+// where it measured faster: the fp64 fixed-point tiles (about 20% at 2^13-element
+// tiles) and the 4-byte 64-byte-segment tiles of 256 threads (about 7%).
+template <class S>
+constexpr int col_tma_min_blocks(int kind) {
+  return (kind == 1 || ((kind == 0 || kind == 2) && S::TS == 4 && S::NT == 256))
+             ? (S::NT < 768 ? 768 / S::NT : 1)
+             : (S::NT < 512 ? 512 / S::NT : 1);
+}
 template <class S, int KIND>
-__global__ void __launch_bounds__(S::NT, KIND == 1 ? (S::NT < 768 ? 768 / S::NT : 1)
-                                                   : (S::NT < 512 ? 512 / S::NT : 1))
+__global__ void __launch_bounds__(S::NT, col_tma_min_blocks<S>(KIND))
     fwt_col_tma_kernel(const __grid_constant__ TmaPassParams tp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bar;
