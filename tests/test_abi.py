@@ -94,11 +94,12 @@ def test_plans(lib):
     assert fwt.plan_factors(24, "c64") == [13, 11]
     if fwt.column_bytes("c32") == 0 and fwt.column_bytes("c64") == 0:
         # measured two-pass splits with narrower column segments for large n
-        assert fwt.plan_factors(27, "c32") == [15, 12]
-        assert fwt.plan_factors(28, "i32") == [15, 13]
+        assert fwt.plan_factors(26, "c32") == [15, 11]
+        assert fwt.plan_factors(27, "c32") == [12, 7, 8]
+        assert fwt.plan_factors(28, "i32") == [13, 8, 7]
         assert fwt.plan_factors(25, "c64") == [14, 11]
         assert fwt.plan_factors(26, "c64") == [12, 6, 8]
-        assert len(fwt.plan_factors(29, "c32")) == 3
+        assert fwt.plan_factors(30, "c64") == [13, 10, 7]
     assert lib.fwt_plan_passes(31, 0) == -1 and lib.fwt_plan_passes(10, 7) == -1
 
 

@@ -112,21 +112,24 @@ bool plan_valid(int n, int dtype, const Plan& p) {
   return sum == n;
 }
 
-// Splits measured faster than the general rule for large vectors (GB300, 2^28
-// elements a part).  4-byte types: narrower column segments let the column factor
-// grow, so n = 27, 28 need two passes instead of three.  fp64: tiles of 2^14
-// elements run one 512-thread CTA an SM and no faster than half the rate of the
-// 2^13-element tiles (three CTAs an SM), so from n = 26 three passes over tiles of
-// at most 2^13 elements (128-byte segments) beat two passes that need one.
+// Splits measured faster than the general rule for large vectors (GB300, a sweep
+// of every split and column width at 2^28 elements a part).  4-byte types: at
+// n = 25, 26 a 32-byte column factor of 11 bits; from n = 27 three passes with
+// 128-byte column segments (each pass near 7 TB/s) beat two passes that need
+// narrow segments.  fp64: tiles of 2^14 elements run one 512-thread CTA an SM and
+// reach about half the rate of the 2^13-element tiles (three CTAs an SM), so from
+// n = 26 three passes over tiles of at most 2^13 elements win.
 struct LargeSplit {
   bool fp64;
   int n, nf, bits[3], col_bytes;
 };
 constexpr LargeSplit kLargeSplits[] = {
-    {false, 25, 2, {14, 11, 0}, 32},  {false, 26, 2, {14, 12, 0}, 32},
-    {false, 27, 2, {15, 12, 0}, 32},  {false, 28, 2, {15, 13, 0}, 16},
-    {true, 25, 2, {14, 11, 0}, 32},   {true, 26, 3, {12, 6, 8}, 128},
-    {true, 27, 3, {12, 7, 8}, 128},   {true, 28, 3, {12, 8, 8}, 128},
+    {false, 25, 2, {14, 11, 0}, 32}, {false, 26, 2, {15, 11, 0}, 32},
+    {false, 27, 3, {12, 7, 8}, 128}, {false, 28, 3, {13, 8, 7}, 128},
+    {false, 29, 3, {13, 8, 8}, 128}, {false, 30, 3, {14, 8, 8}, 128},
+    {true, 25, 2, {14, 11, 0}, 32},  {true, 26, 3, {12, 6, 8}, 128},
+    {true, 27, 3, {12, 7, 8}, 128},  {true, 28, 3, {12, 8, 8}, 128},
+    {true, 29, 3, {12, 10, 7}, 64},  {true, 30, 3, {13, 10, 7}, 64},
 };
 
 Plan default_plan(int n, int dtype) {

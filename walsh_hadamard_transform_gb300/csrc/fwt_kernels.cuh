@@ -347,12 +347,14 @@ template <class S>
 struct StaticBits {
   static constexpr uint32_t r1 = S::RM1, r2 = S::RM2, r3 = S::RM3;
   static constexpr int tk = S::TK;
+  static constexpr int kStaticTk = S::TK;  // transformed bits known at compile time
   __device__ explicit StaticBits(const PassParams&) {}
 };
 template <class S>
 struct RuntimeBits {
   uint32_t r1, r2, r3;
   int tk;
+  static constexpr int kStaticTk = -1;  // transformed bits given at run time
   __device__ explicit RuntimeBits(const PassParams& p) {
     uint32_t rm[3];
     S::round_masks(p.bits_lo, p.bits_k, rm);
@@ -390,25 +392,42 @@ __device__ __forceinline__ uint32_t abs_hi(long long bits) {
   return (uint32_t)((unsigned long long)bits >> 32) & 0x7fffffffu;
 }
 
-// q = round(v * 2^(F + 1023 - emax)), ties away from zero, for |v| < 2^(emax - 1022):
-// |q| <= 2^(F+1).  Integer bit arithmetic only.
-// RIGHT: F <= 51, so every element shifts right by at least one bit (the common
-// case, branch-free, rounding folded into the shift).
-template <bool RIGHT>
+// 64-bit logical right shift with the PTX rule that amounts of 64 or more give 0.
+__device__ __forceinline__ unsigned long long shr64(unsigned long long v, uint32_t s) {
+  unsigned long long r;
+  asm("shr.b64 %0, %1, %2;" : "=l"(r) : "l"(v), "r"(s));
+  return r;
+}
+
+// q = v * 2^(F + 1023 - emax) as an integer, for |v| < 2^(emax - 1022): |q| <= 2^(F+1).
+// Integer bit arithmetic only.  Modes:
+//   TO_FIXED_ANY:   any F (shifts either way), rounded half away from zero.
+//   TO_FIXED_ROUND: F <= 51, so every element shifts right by at least one bit;
+//                   rounded half away from zero (the rounding folded into the shift).
+//   TO_FIXED_TRUNC: F <= 51 and emax >= F + 12, so a zero or subnormal element would
+//                   shift right by 64 bits or more whatever its leading bit: every
+//                   element is taken as a normal number, and the magnitude is
+//                   truncated (error below one unit instead of half a unit).
+enum ToFixedMode { TO_FIXED_ANY, TO_FIXED_ROUND, TO_FIXED_TRUNC };
+template <int MODE>
 __device__ __forceinline__ long long to_fixed(long long bits, int emax, int F) {
   const unsigned long long b = (unsigned long long)bits;
   const int e = (int)((uint32_t)(b >> 32) >> 20) & 0x7ff;
-  const unsigned long long m =
-      (b & 0x000fffffffffffffull) | ((unsigned long long)(e != 0) << 52);
-  // v = m * 2^(max(e,1) - 1075), so q = m * 2^(max(e,1) - emax + F - 52)
-  const int sh = max(e, 1) - emax + F - 52;
   unsigned long long mag;
-  if constexpr (RIGHT) {  // sh <= F - 52 <= -1: shift by rs - 1 >= 0, add the half, halve
-    const int rs1 = min(-sh, 64) - 1;
-    mag = ((m >> rs1) + 1ull) >> 1;
-  } else {  // either way, without a divergent branch: (sh >= 0: rs = 0, exact)
-    const int rs = min(max(-sh, 0), 63);
-    mag = ((((m << 1) >> rs) + 1ull) >> 1) << max(sh, 0);
+  if constexpr (MODE == TO_FIXED_TRUNC) {
+    const unsigned long long m = (b & 0x000fffffffffffffull) | (1ull << 52);
+    mag = shr64(m, (uint32_t)(emax - e + 52 - F));  // >= 1
+  } else {
+    const unsigned long long m =
+        (b & 0x000fffffffffffffull) | ((unsigned long long)(e != 0) << 52);
+    // v = m * 2^(max(e,1) - 1075), so q = m * 2^(max(e,1) - emax + F - 52)
+    const int sh = max(e, 1) - emax + F - 52;
+    if constexpr (MODE == TO_FIXED_ROUND) {  // sh <= -1: shift by -sh - 1, add the half, halve
+      mag = (shr64(m, (uint32_t)(-sh - 1)) + 1ull) >> 1;
+    } else {  // either way, without a divergent branch: (sh >= 0: rs = 0, exact)
+      const int rs = min(max(-sh, 0), 63);
+      mag = ((((m << 1) >> rs) + 1ull) >> 1) << max(sh, 0);
+    }
   }
   const unsigned long long neg = (unsigned long long)((long long)b >> 63);  // 0 or ~0
   return (long long)((mag ^ neg) - neg);
@@ -503,12 +522,24 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
   }
   const int emax = max((int)(key >> 20), 1);  // zeros and subnormals scale as exponent 1
   const int F = 61 - bits.tk;  // headroom: |q| <= 2^(F+1) grows by 2^tk
-  if (F <= 51) {  // (uniform) every element shifts right: the common case
+  // (uniform branches) Tiles of up to 2^13 transformed elements truncate: their error
+  // bound sqrt(T) 2^-F stays far below the fp64 specification; tiles of 2^14 round.
+  bool converted = false;
+  if constexpr (Bits::kStaticTk >= 0 && Bits::kStaticTk <= 13) {
+    if (F <= 51 && emax >= F + 12) {
 #pragma unroll
-    for (int r = 0; r < S::NE; ++r) x[r] = to_fixed<true>(x[r], emax, F);
-  } else {
+      for (int r = 0; r < S::NE; ++r) x[r] = to_fixed<TO_FIXED_TRUNC>(x[r], emax, F);
+      converted = true;
+    }
+  }
+  if (!converted) {
+    if (F <= 51) {
 #pragma unroll
-    for (int r = 0; r < S::NE; ++r) x[r] = to_fixed<false>(x[r], emax, F);
+      for (int r = 0; r < S::NE; ++r) x[r] = to_fixed<TO_FIXED_ROUND>(x[r], emax, F);
+    } else {
+#pragma unroll
+      for (int r = 0; r < S::NE; ++r) x[r] = to_fixed<TO_FIXED_ANY>(x[r], emax, F);
+    }
   }
   tile_rounds<S, ArithI64>(x, reinterpret_cast<long long*>(smem_raw), bits.r1, bits.r2,
                            bits.r3);
