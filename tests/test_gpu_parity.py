@@ -316,3 +316,29 @@ def test_cluster_one_pass(dtype):
                 assert rel_err_per_vector(a[0], a[1], b[0], b[1]).max() < 4e-6
     finally:
         fwt.set_cluster(fwt.CLUSTER_AUTO)
+
+
+@pytest.mark.parametrize("dtype,n", [("c32", 12), ("c64", 24), ("i32", 16), ("c32", 20)])
+def test_cuda_graph_capture_and_replay(dtype, n):
+    """The entry points enqueue only stream work after their first call on a device,
+    so a transform can be captured in a CUDA graph and replayed (launch-bound small
+    batches); each replay must give the oracle's result for the current inputs."""
+    batch = 2 if n >= 20 else 8
+    norm = dtype != "i32"
+    re, im = inputs.random_pair(n, batch, dtype, seed=11)
+    a, b = torch.from_numpy(re).cuda(), torch.from_numpy(im).cuda()
+    c, d = torch.empty_like(a), torch.empty_like(b)
+    fwt.transform(a, b, c, d, normalize=norm)  # device set-up outside the capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fwt.transform(a, b, c, d, normalize=norm)
+    for seed in (12, 13):
+        re2, im2 = inputs.random_pair(n, batch, dtype, seed=seed)
+        a.copy_(torch.from_numpy(re2))
+        b.copy_(torch.from_numpy(im2))
+        g.replay()
+        torch.cuda.synchronize()
+        ore, oim = oracle.fwt_complex(re2, im2, normalize=norm, nthreads=host_threads())
+        assert_matches(dtype, c.cpu().numpy(), d.cpu().numpy(), ore, oim, f"graph replay {dtype} n={n}")
