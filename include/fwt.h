@@ -240,9 +240,13 @@ int fwt_get_tma(void);
  * bits of its slice on chip, and the top bits are transformed across the cluster
  * through distributed shared memory, so the vector costs one HBM read and one
  * write instead of two of each (two Kronecker passes).  mode 1 (default): for
- * n = 15 and 16 (where it measured faster than the factor plans) when the device
- * can hold such a cluster; 2: for every n from 14 to 18; 0: never (factor plans
- * only).  Plans set with fwt_set_plan take precedence.  Returns FWT_OK or
+ * n = 15 .. 17 (where it measured at least as fast as the factor plans) when the
+ * device can hold such a cluster; 2: for every n from 14 to 18; 0: never (factor plans
+ * only).  fp64 uses CTA pairs for 2^14-element vectors (modes 1 and 2), as the
+ * whole transform at n = 14 and as the 14-bit row pass of longer vectors: one
+ * fixed-point exponent over the pair keeps the error bound only up to 2^14
+ * elements.  Plans set with fwt_set_plan take precedence (a 14-bit fp64 row factor
+ * still runs on pairs unless the mode is 0).  Returns FWT_OK or
  * FWT_ERR_INVALID_ARG; fwt_get_cluster returns the mode.
  */
 int fwt_set_cluster(int mode);

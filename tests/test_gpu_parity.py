@@ -342,3 +342,47 @@ def test_cuda_graph_capture_and_replay(dtype, n):
         torch.cuda.synchronize()
         ore, oim = oracle.fwt_complex(re2, im2, normalize=norm, nthreads=host_threads())
         assert_matches(dtype, c.cpu().numpy(), d.cpu().numpy(), ore, oim, f"graph replay {dtype} n={n}")
+
+
+def test_fp64_cluster_pairs():
+    """fp64 vectors of 2^14 elements run one pass on CTA pairs (one fixed-point
+    exponent over the pair); 2^14-element fp64 row passes of longer vectors use the
+    same kernel.  Against the oracle, with the cluster kernel off for comparison,
+    and through its rare paths: Inf/NaN (IEEE adds), a tiny-magnitude vector (exact
+    integer rounding), and values across 1e-300 .. 1e300."""
+    try:
+        assert fwt.plan_passes(14, "c64") == 1
+        for batch, seed in ((1, 1), (3, 2), (64, 3)):
+            for inplace in (False, True):
+                _check("c64", 14, batch, True, seed=seed, inplace=inplace)
+            _check("c64", 14, batch, False, seed=seed + 10)
+        # 2^25 elements: (14, 11), the 14-bit row pass on CTA pairs
+        assert fwt.plan_factors(25, "c64") == [14, 11]
+        _check("c64", 25, 1, True, seed=25)
+        re, im = inputs.random_pair(14, 5, "c64", seed=7)
+        a = gpu_transform(re, im, True)
+        fwt.set_cluster(fwt.CLUSTER_NEVER)
+        assert fwt.plan_passes(14, "c64") == 1
+        b = gpu_transform(re, im, True)
+        assert rel_err_per_vector(a[0], a[1], b[0], b[1]).max() < 2e-12
+    finally:
+        fwt.set_cluster(fwt.CLUSTER_AUTO)
+    n = 14
+    re = np.zeros((2, 1 << n)); im = np.zeros_like(re)
+    re[0, 5] = np.inf; re[1, 8000] = -np.inf; re[1, 9000] = 3.0; im[0, 12000] = np.nan
+    gre, gim = gpu_transform(re, im, False)
+    ore, oim = oracle.fwt_complex(re, im, normalize=False)
+    for g, o in ((gre, ore), (gim, oim)):
+        assert np.array_equal(np.isnan(g), np.isnan(o))
+        fin = ~np.isnan(o)
+        assert np.array_equal(g[fin], o[fin])
+    rng = np.random.default_rng(5)
+    tiny = rng.standard_normal((2, 1 << n)) * 1e-310  # results subnormal: exact path
+    gre, gim = gpu_transform(tiny, tiny[::-1].copy(), True)
+    ore, oim = oracle.fwt_complex(tiny, tiny[::-1].copy(), normalize=True)
+    assert np.array_equal(gre, ore) or rel_err_per_vector(gre, gim, ore, oim).max() <= TOL["c64"]
+    mags = 10.0 ** rng.uniform(-300, 300, size=(2, 1 << n))
+    wide = mags * rng.choice([-1.0, 1.0], size=mags.shape)
+    gre, gim = gpu_transform(wide, wide[::-1].copy(), True)
+    ore, oim = oracle.fwt_complex(wide, wide[::-1].copy(), normalize=True)
+    assert_matches("c64", gre, gim, ore, oim, "cluster pair, wide dynamic range")

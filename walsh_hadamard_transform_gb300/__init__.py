@@ -262,7 +262,8 @@ CLUSTER_NEVER, CLUSTER_AUTO, CLUSTER_FROM_14 = 0, 1, 2
 
 def set_cluster(mode: int) -> None:
     """One-pass cluster transforms of 2^14..2^18-element fp32/int32 vectors:
-    CLUSTER_AUTO (default: n = 15, 16), CLUSTER_FROM_14 (n = 14..18) or CLUSTER_NEVER."""
+    CLUSTER_AUTO (default: 4-byte n = 15..17, fp64 n = 14 on CTA pairs), CLUSTER_FROM_14
+    (4-byte n = 14..18) or CLUSTER_NEVER."""
     st = library().fwt_set_cluster(int(mode))
     if st != FWT_OK:
         raise FwtError(st, f"fwt_set_cluster({mode})")

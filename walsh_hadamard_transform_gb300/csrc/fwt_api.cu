@@ -178,6 +178,11 @@ Plan default_plan(int n, int dtype) {
   return p;
 }
 
+int cluster_mode() {
+  std::lock_guard<std::mutex> lk(g_plan_mu);
+  return g_use_cluster;
+}
+
 Plan get_plan(int n, int dtype) {
   int mode;
   {
@@ -188,10 +193,15 @@ Plan get_plan(int n, int dtype) {
   }
   Plan p = default_plan(n, dtype);
   // a vector of 2^14 .. 2^18 4-byte elements in one pass on a thread-block cluster
-  // (slices of 2^14, else 2^15 or 2^13).  Measured on GB300 against the two-pass
-  // plans: faster for n = 15, 16 (clusters of 2 and 4 CTAs), even at 17, slower at
-  // 18 (16-CTA clusters), so the default uses it for n = 15, 16 only.
-  const int lo_n = mode == 2 ? 14 : 15, hi_n = mode == 2 ? 18 : 16;
+  // (slices of 2^14, else 2^15 or 2^13).  Measured on GB300 against the factor
+  // plans: faster for n = 16, 17 (clusters of 4 and 8 CTAs: 0.23 vs 0.32 ms and
+  // 0.29 vs 0.32 ms at 2^26 elements), even at 15, slower at 18 (16-CTA clusters),
+  // so the default uses it for n = 15 .. 17.
+  const int lo_n = mode == 2 ? 14 : 15, hi_n = mode == 2 ? 18 : 17;
+  if (dtype == FWT_C64 && mode > 0 && n == 14) {  // fp64: CTA pairs, 2^13-element slices
+    const KernelEntry* e = find_kernel(dtype, KIND_CLUSTER, 14, 13);
+    if (e && cluster_runnable(e)) p.cluster = e;
+  }
   if (dtype != FWT_C64 && mode > 0 && n >= lo_n && n <= hi_n) {
     for (int tb : {14, 15, 13}) {
       if (n - tb < 1 || n - tb > 4) continue;
@@ -330,7 +340,14 @@ bool full_passes(int n, int dtype, const Plan& plan, std::vector<PassSpec>& out)
   for (int f = 0; f < plan.nf; ++f) {
     const int K = plan.bits[f];
     PassSpec ps{nullptr, L, 0, 0};
-    if (f == 0) ps.e = find_kernel(dtype, K <= 2 ? KIND_SMALL : KIND_ROW, K);
+    if (f == 0 && dtype == FWT_C64 && K == 14 && cluster_mode() > 0) {
+      // fp64 row tiles of 2^14 elements: a CTA pair (three CTAs an SM) instead of
+      // one 512-thread CTA holding the whole tile
+      const KernelEntry* c = find_kernel(dtype, KIND_CLUSTER, 14, 13);
+      if (c && cluster_runnable(c)) ps.e = c;
+    }
+    if (ps.e) {  // chosen above
+    } else if (f == 0) ps.e = find_kernel(dtype, K <= 2 ? KIND_SMALL : KIND_ROW, K);
     else ps.e = find_kernel(dtype, KIND_COL, K, plan.col_bytes, col_tma(plan, K));
     if (!ps.e) return false;
     out.push_back(ps);

@@ -629,13 +629,18 @@ __global__ void __launch_bounds__(S::NT, col_tma_min_blocks<S>(KIND))
 // ---- one-pass transform of a vector spread over a thread-block cluster -----------------
 // A vector of 2^n elements, n = TB + CL, is held by a cluster of 2^CL CTAs, CTA r
 // owning the contiguous slice [r 2^TB, (r+1) 2^TB).  Each CTA transforms the low TB
-// index bits of its slice with the tile engine, writes the result into its shared
-// memory in natural order, and after a cluster barrier transforms the top CL bits
-// across the cluster: CTA r reads, for its share of slice positions i, the element
-// at i of every CTA's slice from distributed shared memory (ld.shared::cluster),
-// runs the CL butterfly stages in registers and writes the 2^CL outputs.  The whole
-// transform costs one HBM read and one write of each element (the second Kronecker
-// factor moves over the cluster's shared memory instead of HBM).
+// index bits of its slice with the tile engine.  CTA s then finishes the slice
+// positions [s M, (s+1) M), M = 2^TB / 2^CL: it gathers the elements of all 2^CL
+// slices at those positions through distributed shared memory, runs the CL
+// butterfly stages in registers and writes the 2^CL outputs.  The gather is a pull
+// (each CTA parks its slice in its own shared memory; after a cluster barrier CTA s
+// reads the positions from every CTA, ld.shared::cluster; a last barrier keeps the
+// slices alive until all reads are done) or, for large clusters, a push (after a
+// barrier every CTA stores its elements straight into the finishing CTAs' shared
+// memory, st.shared::cluster, slot r of s's buffer; after a second barrier CTA s
+// reads its positions locally).  The whole transform costs one HBM read and one
+// write of each element (the second Kronecker factor moves over the cluster's
+// shared memory instead of HBM).
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -645,6 +650,52 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
 }
+// 16-byte store into the shared memory of CTA `rank` of the cluster, at the same
+// offset as `local` in this CTA.
+__device__ __forceinline__ void st_dsmem16(void* local, uint32_t rank, const uint4& v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(remote), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Hands this CTA's transformed slice (layout L3) to the CTAs that finish it: the
+// element at slice position i goes to CTA s = i / M, into slot `rank` of s's buffer
+// (element rank M + i mod M).  A warp's 16-byte vectors are 512 contiguous bytes of
+// one slice, so each store instruction goes to one CTA, conflict-free.
+template <class S, int CL, typename U>
+__device__ __forceinline__ void push_to_owners(const U (&x)[S::NE], U* sm, uint32_t rank) {
+  constexpr int M = 1 << (S::TB - CL);
+  using V = typename Vec16<U>::type;
+#pragma unroll
+  for (int j = 0; j < S::NV; ++j) {
+    const uint32_t i = S::idx3(threadIdx.x, j * S::VEC);
+    const uint32_t owner = i >> (S::TB - CL);  // uniform over the warp
+    U* dst = sm + rank * M + (i & (M - 1));
+    V v;
+    U* pv = reinterpret_cast<U*>(&v);
+#pragma unroll
+    for (int e = 0; e < S::VEC; ++e) pv[e] = x[j * S::VEC + e];
+    if (owner == rank) *reinterpret_cast<V*>(dst) = v;
+    else st_dsmem16(dst, owner, *reinterpret_cast<const uint4*>(&v));
+  }
+}
+
+// The 2^CL slices' elements at this CTA's 16-byte position j (offset within its
+// share), from its own buffer after the push.
+template <int C, int M, int VEC, typename U>
+__device__ __forceinline__ void gather_share(const U* sm, uint32_t j, U (&y)[C * VEC]) {
+  using V = typename Vec16<U>::type;
+#pragma unroll
+  for (int r = 0; r < C; ++r) {
+    const V v = *reinterpret_cast<const V*>(sm + r * M + j);
+    const U* pv = reinterpret_cast<const U*>(&v);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) y[r * VEC + e] = pv[e];
+  }
+}
+
 // 16-byte load from the shared memory of CTA `rank` of the cluster, at the same
 // offset as `local` in this CTA.
 __device__ __forceinline__ uint4 ld_dsmem16(const void* local, uint32_t rank) {
@@ -658,16 +709,159 @@ __device__ __forceinline__ uint4 ld_dsmem16(const void* local, uint32_t rank) {
   return v;
 }
 
+// The 2^CL slices' elements at slice position i, read from every CTA's parked slice.
+template <int C, int VEC, typename U>
+__device__ __forceinline__ void gather_remote(const U* sm, uint32_t i, U (&y)[C * VEC]) {
+#pragma unroll
+  for (int r = 0; r < C; ++r) {
+    const uint4 v = ld_dsmem16(sm + i, (uint32_t)r);
+    const U* pv = reinterpret_cast<const U*>(&v);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) y[r * VEC + e] = pv[e];
+  }
+}
+
+// Layout L3 back to the tile buffer in natural order (after the engine's last reads).
+template <class S, typename U>
+__device__ __forceinline__ void park_natural(const U (&x)[S::NE], U* sm) {
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < S::NV; ++j) put_vec<U, S::VEC>(sm + S::idx3(threadIdx.x, j * S::VEC), x, j);
+}
+
+// 32-bit load from the shared memory of CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t ld_dsmem32(const void* local, uint32_t rank) {
+  uint32_t remote, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// fp64 one-pass on a cluster of 2^CL CTAs, in exact fixed point: one binary
+// exponent for the whole 2^(TB+CL)-element vector (the largest over the cluster),
+// each slice transformed in int64 by the tile engine, the top CL bits across the
+// cluster, one rounding to fp64 on the way out.  The vector has F = 61 - (TB + CL)
+// fraction bits, so the per-pass bound sqrt(2^(TB+CL)) 2^-(F+1) stays below 1e-12
+// only for TB + CL <= 14: the registry builds it for TB = 13, CL = 1.  Every CTA
+// takes every cluster barrier whatever happens (a slice whose bulk copy gave up
+// computes on zeros and stores nothing), so no CTA waits on one that left.
+template <class S, int CL>
+__device__ __forceinline__ void cluster_fixed_body(const PassParams& p, unsigned char* smem_raw,
+                                                   uint64_t* bar) {
+  constexpr int C = 1 << CL;
+  constexpr int M = 1 << (S::TB - CL);            // slice positions each CTA finishes
+  constexpr int GROUPS = M / S::VEC / S::NT;      // 16-byte positions a thread finishes
+  static_assert(GROUPS >= 1, "each thread finishes at least one 16-byte position");
+  static_assert(S::TB + CL <= 14, "the fixed-point error bound needs vectors of <= 2^14");
+  __shared__ uint32_t red[32];
+  __shared__ uint32_t slice_key;
+  long long* sm = reinterpret_cast<long long*>(smem_raw);
+  const uint32_t t = threadIdx.x;
+  const uint32_t rank = cluster_ctarank();
+  const long long vbase = ((long long)blockIdx.x >> CL) << (S::TB + CL);
+  long long* out = static_cast<long long*>(blockIdx.y != 0 ? p.out[1] : p.out[0]);
+
+  BulkMover<S> mv(p, smem_raw, bar);
+  long long x[S::NE];
+  const bool loaded = mv.load(x, p.ld_policy);
+  if (!loaded) {
+#pragma unroll
+    for (int r = 0; r < S::NE; ++r) x[r] = 0;
+  }
+  // largest exponent of the slice, then of the vector
+  uint32_t key = 0;
+#pragma unroll
+  for (int r = 0; r < S::NE; ++r) key = max(key, abs_hi(x[r]));
+  key = __reduce_max_sync(0xffffffffu, key);
+  if ((t & 31u) == 0) red[t >> 5] = key;
+  __syncthreads();
+  if (t == 0) {
+    uint32_t k = red[0];
+#pragma unroll
+    for (int w = 1; w < S::NT / 32; ++w) k = max(k, red[w]);
+    slice_key = k;
+  }
+  cluster_sync_all();  // every slice's key is visible to the cluster
+  key = 0;
+#pragma unroll
+  for (int r = 0; r < C; ++r) key = max(key, ld_dsmem32(&slice_key, (uint32_t)r));
+  const unsigned long long pol = l2_policy(p.st_policy);
+
+  if (key >= 0x7ff00000u) {  // rare (cluster-uniform): Inf/NaN take plain IEEE fp64 adds
+    double xd[S::NE];
+#pragma unroll
+    for (int r = 0; r < S::NE; ++r) xd[r] = __longlong_as_double(x[r]);
+    double* smd = reinterpret_cast<double*>(sm);
+    tile_rounds<S, ArithF64>(xd, smd);
+    park_natural<S>(xd, smd);
+    cluster_sync_all();  // every slice is in its CTA's shared memory
+#pragma unroll 2
+    for (int q = 0; q < GROUPS; ++q) {
+      const uint32_t i = rank * M + (t + q * S::NT) * S::VEC;
+      double y[C * S::VEC];
+      gather_remote<C, S::VEC>(smd, i, y);
+      butterflies<ArithF64>(y, (uint32_t)(C - 1) << S::LV);
+      if (p.do_scale) {
+#pragma unroll
+        for (int e = 0; e < C * S::VEC; ++e) y[e] = y[e] * p.scale_f64;
+      }
+      if (loaded) {
+#pragma unroll
+        for (int r = 0; r < C; ++r) {
+          double2 v = make_double2(y[r * S::VEC], y[r * S::VEC + 1]);
+          stg16<double>(out + vbase + ((long long)r << S::TB) + i, v, pol);
+        }
+      }
+    }
+    cluster_sync_all();  // no CTA leaves while others still read its shared memory
+    return;
+  }
+
+  const int emax = max((int)(key >> 20), 1);
+  constexpr int F = 61 - (S::TB + CL);
+  static_assert(F <= 51, "vectors this long always shift right");
+#pragma unroll
+  for (int r = 0; r < S::NE; ++r) x[r] = to_fixed<TO_FIXED_ROUND>(x[r], emax, F);
+  tile_rounds<S, ArithI64>(x, sm);
+  park_natural<S>(x, sm);
+  cluster_sync_all();  // every slice is in its CTA's shared memory
+  const int e0 = emax - 1023 - F + (p.do_scale ? p.scale_exp : 0);
+  const int half = p.do_scale ? p.scale_half : 0;
+  const bool normal = e0 >= -1022 && e0 <= 960;  // results are normal numbers (uniform)
+  const long long e0_field = (long long)((unsigned long long)(long long)e0 << 52);
+#pragma unroll 2
+  for (int q = 0; q < GROUPS; ++q) {
+    const uint32_t i = rank * M + (t + q * S::NT) * S::VEC;
+    long long y[C * S::VEC];
+    gather_remote<C, S::VEC>(sm, i, y);
+    butterflies<ArithI64>(y, (uint32_t)(C - 1) << S::LV);
+    if (normal) {
+#pragma unroll
+      for (int e = 0; e < C * S::VEC; ++e) y[e] = from_fixed_cvt(y[e], e0_field, half, p.rsqrt2_q64);
+    } else {
+#pragma unroll 1
+      for (int e = 0; e < C * S::VEC; ++e) y[e] = from_fixed_exact(y[e], e0, half, p.rsqrt2_q64);
+    }
+    if (loaded) {
+#pragma unroll
+      for (int r = 0; r < C; ++r) {
+        longlong2 v = make_longlong2(y[r * S::VEC], y[r * S::VEC + 1]);
+        stg16<long long>(out + vbase + ((long long)r << S::TB) + i, v, pol);
+      }
+    }
+  }
+  cluster_sync_all();  // no CTA leaves while others still read its shared memory
+}
+
+// fp32 / int32 body of the cluster kernel (see above).
 template <class S, int KIND, int CL>
-__global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
-    fwt_cluster_kernel(const PassParams p) {
+__device__ __forceinline__ void cluster_plain_body(const PassParams& p, unsigned char* smem_raw) {
   using T = typename std::conditional<KIND == 0, float, uint32_t>::type;
   using A = typename std::conditional<KIND == 0, ArithF32, ArithU32>::type;
   constexpr int C = 1 << CL;
   constexpr int M = 1 << (S::TB - CL);  // slice positions each CTA finishes
   constexpr int GROUPS = M / S::VEC / S::NT;  // 16-byte positions a thread finishes
   static_assert(GROUPS >= 1, "each thread finishes at least one 16-byte position");
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
   T* sm = reinterpret_cast<T*>(smem_raw);
   const uint32_t t = threadIdx.x;
   const uint32_t rank = cluster_ctarank();
@@ -685,24 +879,27 @@ __global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
   T x[S::NE];
   load_tile<S>(in, m, x, p.ld_policy);
   tile_rounds<S, A>(x, sm);
-  __syncthreads();  // the engine's last reads of the buffer are done
-#pragma unroll
-  for (int j = 0; j < S::NV; ++j) put_vec<T, S::VEC>(sm + S::idx3(t, j * S::VEC), x, j);
-  cluster_sync_all();  // every slice is in its CTA's shared memory
+  // Clusters of up to 4 CTAs pull the other slices' elements from their CTAs'
+  // shared memory; larger ones, where remote loads would keep many more requests in
+  // flight for each thread, push their elements to the finishing CTAs instead
+  // (measured: pull faster at 2 and 4 CTAs, push at 8 and 16).
+  constexpr bool kPush = C >= 8;
+  if constexpr (kPush) {
+    cluster_sync_all();  // every CTA is done with its buffer; the peers write into it next
+    push_to_owners<S, CL>(x, sm, rank);
+  } else {
+    park_natural<S>(x, sm);
+  }
+  cluster_sync_all();  // every share (push) or slice (pull) is in place
 
-  // top CL bits across the cluster
+  // top CL bits of this CTA's share
   const unsigned long long pol = l2_policy(p.st_policy);
 #pragma unroll
   for (int q = 0; q < GROUPS; ++q) {
-    const uint32_t i = rank * M + (t + q * S::NT) * S::VEC;  // slice position of this group
+    const uint32_t j = (t + q * S::NT) * S::VEC, i = rank * M + j;  // share offset, slice position
     T y[C * S::VEC];
-#pragma unroll
-    for (int r = 0; r < C; ++r) {
-      const uint4 v = ld_dsmem16(sm + i, (uint32_t)r);
-      const T* pv = reinterpret_cast<const T*>(&v);
-#pragma unroll
-      for (int e = 0; e < S::VEC; ++e) y[r * S::VEC + e] = pv[e];
-    }
+    if constexpr (kPush) gather_share<C, M, S::VEC>(sm, j, y);
+    else gather_remote<C, S::VEC>(sm, i, y);
     butterflies<A>(y, (uint32_t)(C - 1) << S::LV);
     if constexpr (KIND == 0) {
       if (p.do_scale) {
@@ -719,7 +916,22 @@ __global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
       stg16<T>(out + vbase + ((long long)r << S::TB) + i, v, pol);
     }
   }
-  cluster_sync_all();  // no CTA leaves while others still read its shared memory
+  if constexpr (!kPush) cluster_sync_all();  // no CTA leaves while others still read its shared memory
+}
+
+// 4-byte types: 512 threads an SM at up to 128 registers; fp64 fixed point: 768 at 80.
+template <class S, int KIND, int CL>
+__global__ void __launch_bounds__(S::NT, (S::NT < (KIND == 1 ? 768 : 512)
+                                              ? (KIND == 1 ? 768 : 512) / S::NT
+                                              : 1))
+    fwt_cluster_kernel(const PassParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  if constexpr (KIND == 1) {
+    __shared__ __align__(8) uint64_t bar;
+    cluster_fixed_body<S, CL>(p, smem_raw, &bar);
+  } else {
+    cluster_plain_body<S, KIND, CL>(p, smem_raw);
+  }
 }
 
 // ---- fused diagonal phase + transform (first pass, fp32) ----------------------------

@@ -413,7 +413,7 @@ cudaError_t launch_cluster(const PassParams& p, long long tiles, int ncomp, cuda
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)tiles, (unsigned)ncomp, 1);
   cfg.blockDim = dim3(S::NT, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)4 << S::TB;
+  cfg.dynamicSmemBytes = (size_t)(KIND == 1 ? 8 : 4) << S::TB;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -428,7 +428,7 @@ template <class S, int KIND, int CL>
 cudaError_t setup_cluster() {
   cudaError_t err = cudaFuncSetAttribute(fwt_cluster_kernel<S, KIND, CL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)((size_t)4 << S::TB));
+                                         (int)((size_t)(KIND == 1 ? 8 : 4) << S::TB));
   if (err == cudaSuccess && CL > 3)
     err = cudaFuncSetAttribute(fwt_cluster_kernel<S, KIND, CL>,
                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -440,7 +440,7 @@ int cluster_capacity() {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1u << CL, 1, 1);
   cfg.blockDim = dim3(S::NT, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)4 << S::TB;
+  cfg.dynamicSmemBytes = (size_t)(KIND == 1 ? 8 : 4) << S::TB;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1u << CL;
@@ -457,14 +457,16 @@ int cluster_capacity() {
 }
 
 // One-pass transform of 2^(TB + CL)-element vectors on clusters of 2^CL CTAs
-// (fp32 / int32).  K = TB + CL is the vector's n.
+// (fp32 / int32, and fp64 fixed point for TB + CL = 14).  K = TB + CL is the
+// vector's n.
 template <int DT, int KIND, int TB, int CL>
 KernelEntry cluster_entry() {
-  constexpr int EL = choose_el(TB, 2);
-  using S = Shape<TB, 0, TB, 2, TB - EL>;
+  constexpr int LV = KIND == 1 ? 1 : 2;
+  constexpr int EL = choose_el(TB, LV);
+  using S = Shape<TB, 0, TB, LV, TB - EL>;
   KernelEntry e;
   e.dtype = DT; e.kind = KIND_CLUSTER; e.K = TB + CL; e.TB = TB; e.TS = CL; e.col_bytes = 0;
-  e.tma = 0; e.threads = S::NT; e.smem = (size_t)4 << TB;
+  e.tma = 0; e.threads = S::NT; e.smem = (size_t)(KIND == 1 ? 8 : 4) << TB;
   e.launch = &launch_cluster<S, KIND, CL>;
   e.setup = &setup_cluster<S, KIND, CL>;
   e.selfcheck = [] { return check_shape<S, false>("cluster slice"); };
