@@ -175,6 +175,28 @@ int fwt_host_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, in
  */
 size_t fwt_host_workspace_bytes(int dtype, int n, int64_t batch, int with_im);
 
+/*
+ * fwt_host_* without a caller workspace: the staging buffer is the library's own
+ * static device memory, a file-scope __device__ array of
+ * fwt_host_static_workspace_bytes() bytes per device that is part of the module
+ * image (set up with cudaGetSymbolAddress on first use on a device), so nothing is
+ * allocated at run time.  The pages have no counterpart of this entry point: it is
+ * a convenience of the host-buffer path.  Same operation, arguments, layout,
+ * in-place rules, asynchrony and errors as fwt_host_*; a vector (both parts) larger
+ * than the static buffer is FWT_ERR_INVALID_ARG.  Calls share the buffer: each call
+ * makes `stream` wait until the previous call (any stream, same device) has copied
+ * its last chunk out.
+ */
+int fwt_host_static_c32(const float* re_in, const float* im_in, float* re_out, float* im_out,
+                        int n, int64_t batch, int normalize, fwt_stream_t stream);
+int fwt_host_static_c64(const double* re_in, const double* im_in, double* re_out,
+                        double* im_out, int n, int64_t batch, int normalize,
+                        fwt_stream_t stream);
+int fwt_host_static_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out,
+                        int32_t* im_out, int n, int64_t batch, int normalize,
+                        fwt_stream_t stream);
+size_t fwt_host_static_workspace_bytes(void);
+
 /* Static text for a status code (never NULL). */
 const char* fwt_status_string(int status);
 

@@ -66,6 +66,12 @@ def library() -> ctypes.CDLL:
             f.restype = ci
         lib.fwt_host_workspace_bytes.argtypes = [ci, ci, i64, ci]
         lib.fwt_host_workspace_bytes.restype = ctypes.c_size_t
+        for name in ("fwt_host_static_c32", "fwt_host_static_c64", "fwt_host_static_i32"):
+            f = getattr(lib, name)
+            f.argtypes = [vp, vp, vp, vp, ci, i64, ci, vp]
+            f.restype = ci
+        lib.fwt_host_static_workspace_bytes.argtypes = []
+        lib.fwt_host_static_workspace_bytes.restype = ctypes.c_size_t
         lib.fwt_status_string.argtypes = [ci]
         lib.fwt_status_string.restype = ctypes.c_char_p
         lib.fwt_last_cuda_error.argtypes = []
@@ -159,6 +165,25 @@ def fwt_host_i32(re_in, im_in, re_out, im_out, n, batch, normalize, workspace, w
                  stream) -> int:
     return library().fwt_host_i32(re_in, im_in, re_out, im_out, n, batch, int(normalize),
                                   workspace, workspace_bytes, stream)
+
+
+def fwt_host_static_c32(re_in, im_in, re_out, im_out, n, batch, normalize, stream) -> int:
+    return library().fwt_host_static_c32(re_in, im_in, re_out, im_out, n, batch, int(normalize),
+                                         stream)
+
+
+def fwt_host_static_c64(re_in, im_in, re_out, im_out, n, batch, normalize, stream) -> int:
+    return library().fwt_host_static_c64(re_in, im_in, re_out, im_out, n, batch, int(normalize),
+                                         stream)
+
+
+def fwt_host_static_i32(re_in, im_in, re_out, im_out, n, batch, normalize, stream) -> int:
+    return library().fwt_host_static_i32(re_in, im_in, re_out, im_out, n, batch, int(normalize),
+                                         stream)
+
+
+def fwt_host_static_workspace_bytes() -> int:
+    return int(library().fwt_host_static_workspace_bytes())
 
 
 def fwt_host_workspace_bytes(dtype, n, batch, with_im=True) -> int:

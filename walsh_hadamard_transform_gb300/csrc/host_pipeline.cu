@@ -197,3 +197,87 @@ int fwt_host_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, in
 }
 
 }  // extern "C"
+
+// ---- host-buffer entry points with a static device workspace -------------------------
+// The same pipeline over a workspace that is part of the module image: a file-scope
+// device array (allocated with the module when it loads, one per device), found with
+// cudaGetSymbolAddress.  The library allocates nothing at run time.  Calls share the
+// buffer, so each one first waits (on the caller's stream) for the previous one to
+// have copied its last chunk out.
+namespace fwt {
+namespace {
+
+constexpr size_t kStaticWorkspaceBytes = 512ull << 20;
+static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
+
+struct StaticWorkspace {
+  void* ptr = nullptr;
+  cudaEvent_t done = nullptr;  // recorded on the caller's stream after each call
+  bool used = false;
+};
+std::mutex g_static_mu;  // taken before g_mu, never after it
+std::vector<StaticWorkspace> g_static;
+
+int run_host_static(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out,
+                    int n, int64_t batch, int normalize, cudaStream_t stream) {
+  // argument errors before any CUDA call (the pipeline repeats the full checks)
+  if (n < 0 || n > 30 || batch < 0) return FWT_ERR_INVALID_ARG;
+  if (batch == 0) return FWT_OK;
+  if (!re_in || !re_out || (!im_in) != (!im_out)) return FWT_ERR_INVALID_ARG;
+  if (!im_in && dtype != FWT_I32) return FWT_ERR_INVALID_ARG;
+  if (dtype == FWT_I32 && normalize) return FWT_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess && (int)g_static.size() <= dev) g_static.resize(dev + 1);
+  StaticWorkspace* sw = err == cudaSuccess ? &g_static[dev] : nullptr;
+  if (err == cudaSuccess && !sw->ptr) {
+    err = cudaGetSymbolAddress(&sw->ptr, g_static_workspace);
+    if (err == cudaSuccess) err = cudaEventCreateWithFlags(&sw->done, cudaEventDisableTiming);
+    if (err != cudaSuccess) sw->ptr = nullptr;
+  }
+  if (err == cudaSuccess && sw->used) err = cudaStreamWaitEvent(stream, sw->done, 0);
+  if (err != cudaSuccess) {
+    set_last_cuda_error((int)err);
+    return FWT_ERR_CUDA;
+  }
+  const int st = run_host(dtype, re_in, im_in, re_out, im_out, n, batch, normalize, sw->ptr,
+                          kStaticWorkspaceBytes, stream);
+  if (st != FWT_OK) return st;
+  err = cudaEventRecord(sw->done, stream);
+  if (err != cudaSuccess) {
+    set_last_cuda_error((int)err);
+    return FWT_ERR_CUDA;
+  }
+  sw->used = true;
+  return FWT_OK;
+}
+
+}  // namespace
+}  // namespace fwt
+
+extern "C" {
+
+size_t fwt_host_static_workspace_bytes(void) { return fwt::kStaticWorkspaceBytes; }
+
+int fwt_host_static_c32(const float* re_in, const float* im_in, float* re_out, float* im_out,
+                        int n, int64_t batch, int normalize, fwt_stream_t stream) {
+  return fwt::run_host_static(FWT_C32, re_in, im_in, re_out, im_out, n, batch, normalize,
+                              (cudaStream_t)stream);
+}
+
+int fwt_host_static_c64(const double* re_in, const double* im_in, double* re_out,
+                        double* im_out, int n, int64_t batch, int normalize,
+                        fwt_stream_t stream) {
+  return fwt::run_host_static(FWT_C64, re_in, im_in, re_out, im_out, n, batch, normalize,
+                              (cudaStream_t)stream);
+}
+
+int fwt_host_static_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out,
+                        int32_t* im_out, int n, int64_t batch, int normalize,
+                        fwt_stream_t stream) {
+  return fwt::run_host_static(FWT_I32, re_in, im_in, re_out, im_out, n, batch, normalize,
+                              (cudaStream_t)stream);
+}
+
+}  // extern "C"
