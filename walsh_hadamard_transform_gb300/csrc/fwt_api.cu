@@ -318,7 +318,10 @@ const KernelEntry* column_kernel(int dtype, int K, int L, const Plan& plan) {
 // allows (near-equal sizes).
 bool column_passes(int dtype, int L, int hi, const Plan& plan, std::vector<PassSpec>& out) {
   const int rest = hi - L;
-  const int cmax = max_col_bits(dtype, plan.col_bytes);
+  // fp64 column tiles of 2^14 elements run one 512-thread CTA an SM at about half
+  // the rate of smaller ones: split into more factors instead (tiles <= 2^13)
+  const int cmax = std::min(max_col_bits(dtype, plan.col_bytes),
+                            dtype == FWT_C64 ? min_col_bits(dtype, plan.col_bytes) + 3 : 30);
   const int nf = (rest + cmax - 1) / cmax;
   for (int f = 0; f < nf; ++f) {
     const int K = rest / nf + (f < rest % nf ? 1 : 0);
@@ -558,6 +561,13 @@ int run_phase(const float* re_in, const float* im_in, const float* theta, int64_
   Plan plan = default_plan(n, FWT_C32);
   if (plan.tma && !tensor_map_encoder()) plan.tma = 0;
   const int k1 = std::min(n, 13);
+  {
+    // the fused first pass covers 13 bits, so 11- and 12-bit column factors follow;
+    // at 64-byte segments they need 512-thread tiles, at 32 bytes 256 (measured 1.07
+    // vs 0.82 ms at n = 24, batch 16)
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    if (g_col_bytes[FWT_C32] == 0 && n - k1 >= 11 && n - k1 <= 12) plan.col_bytes = 32;
+  }
   std::vector<PassSpec> passes;
   const KernelEntry* e0 = find_kernel(FWT_C32, KIND_PHASE, k1);
   if (!e0) return FWT_ERR_UNSUPPORTED;

@@ -347,14 +347,14 @@ template <class S>
 struct StaticBits {
   static constexpr uint32_t r1 = S::RM1, r2 = S::RM2, r3 = S::RM3;
   static constexpr int tk = S::TK;
-  static constexpr int kStaticTk = S::TK;  // transformed bits known at compile time
+  static constexpr bool kMayTruncate = S::TK <= 13;  // transformed bits known at compile time
   __device__ explicit StaticBits(const PassParams&) {}
 };
 template <class S>
 struct RuntimeBits {
   uint32_t r1, r2, r3;
   int tk;
-  static constexpr int kStaticTk = -1;  // transformed bits given at run time
+  static constexpr bool kMayTruncate = true;  // decided at run time from tk
   __device__ explicit RuntimeBits(const PassParams& p) {
     uint32_t rm[3];
     S::round_masks(p.bits_lo, p.bits_k, rm);
@@ -476,10 +476,12 @@ __device__ __forceinline__ long long from_fixed_exact(long long q, int e0, int h
 // nearest even; it runs on the fp64 unit, beside the integer pipes), followed by an
 // exact power-of-two rescale done as an add to the exponent field.  Valid when
 // every nonzero result is a normal number: -1022 <= e0 <= 960 (|q| < 2^63).
-// e0_field = e0 << 52.  `half` (uniform) also divides by sqrt(2) first.
-__device__ __forceinline__ long long from_fixed_cvt(long long q, long long e0_field, int half,
+// e0_field = e0 << 52.  HALF also divides by sqrt(2) first (a compile-time choice,
+// so the unrolled per-element code carries no predicated-off multiply).
+template <bool HALF>
+__device__ __forceinline__ long long from_fixed_cvt(long long q, long long e0_field,
                                                     unsigned long long rsqrt2) {
-  if (half) {
+  if constexpr (HALF) {
     const unsigned long long neg = (unsigned long long)(q >> 63);
     const unsigned long long a = __umul64hi(((unsigned long long)q ^ neg) - neg, rsqrt2);
     q = (long long)((a ^ neg) - neg);
@@ -525,8 +527,8 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
   // (uniform branches) Tiles of up to 2^13 transformed elements truncate: their error
   // bound sqrt(T) 2^-F stays far below the fp64 specification; tiles of 2^14 round.
   bool converted = false;
-  if constexpr (Bits::kStaticTk >= 0 && Bits::kStaticTk <= 13) {
-    if (F <= 51 && emax >= F + 12) {
+  if constexpr (Bits::kMayTruncate) {
+    if (bits.tk <= 13 && F <= 51 && emax >= F + 12) {
 #pragma unroll
       for (int r = 0; r < S::NE; ++r) x[r] = to_fixed<TO_FIXED_TRUNC>(x[r], emax, F);
       converted = true;
@@ -549,8 +551,13 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
   // 1 <= e0 + 1023 and e0 + 1023 + 63 <= 2046 (uniform over the tile)
   if (e0 >= -1022 && e0 <= 960) {
     const long long e0_field = (long long)((unsigned long long)(long long)e0 << 52);
+    if (half) {
 #pragma unroll
-    for (int r = 0; r < S::NE; ++r) x[r] = from_fixed_cvt(x[r], e0_field, half, p.rsqrt2_q64);
+      for (int r = 0; r < S::NE; ++r) x[r] = from_fixed_cvt<true>(x[r], e0_field, p.rsqrt2_q64);
+    } else {
+#pragma unroll
+      for (int r = 0; r < S::NE; ++r) x[r] = from_fixed_cvt<false>(x[r], e0_field, p.rsqrt2_q64);
+    }
   } else {  // rare: a rolled loop over a local copy keeps this code small
     long long xl[S::NE];
 #pragma unroll
@@ -593,6 +600,17 @@ __global__ void __launch_bounds__(S::NT, KIND == 1 ? (S::NT < 768 ? 768 / S::NT 
   __shared__ __align__(8) uint64_t bar;
   BulkMover<S> mv(p, smem_raw, &bar);
   tile_body<S, KIND>(p, smem_raw, mv, StaticBits<S>(p));
+}
+
+// The same over bulk-copied whole tiles (fp64 fixed point: three CTAs an SM).
+template <class S, int KIND>
+__global__ void __launch_bounds__(S::NT, KIND == 1 ? (S::NT < 768 ? 768 / S::NT : 1)
+                                                   : (S::NT < 512 ? 512 / S::NT : 1))
+    fwt_rowbits_bulk_kernel(const PassParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ __align__(8) uint64_t bar;
+  BulkMover<S> mv(p, smem_raw, &bar);
+  tile_body<S, KIND>(p, smem_raw, mv, RuntimeBits<S>(p));
 }
 
 // Contiguous tiles of 2^TB elements whose transformed bits [bits_lo, bits_lo +
@@ -837,7 +855,9 @@ __device__ __forceinline__ void cluster_fixed_body(const PassParams& p, unsigned
     butterflies<ArithI64>(y, (uint32_t)(C - 1) << S::LV);
     if (normal) {
 #pragma unroll
-      for (int e = 0; e < C * S::VEC; ++e) y[e] = from_fixed_cvt(y[e], e0_field, half, p.rsqrt2_q64);
+      for (int e = 0; e < C * S::VEC; ++e)
+        y[e] = half ? from_fixed_cvt<true>(y[e], e0_field, p.rsqrt2_q64)
+                    : from_fixed_cvt<false>(y[e], e0_field, p.rsqrt2_q64);
     } else {
 #pragma unroll 1
       for (int e = 0; e < C * S::VEC; ++e) y[e] = from_fixed_exact(y[e], e0, half, p.rsqrt2_q64);
@@ -919,11 +939,10 @@ __device__ __forceinline__ void cluster_plain_body(const PassParams& p, unsigned
   if constexpr (!kPush) cluster_sync_all();  // no CTA leaves while others still read its shared memory
 }
 
-// 4-byte types: 512 threads an SM at up to 128 registers; fp64 fixed point: 768 at 80.
+// 768 threads an SM at up to 80 registers: a third resident CTA per SM measured
+// 2-10% faster than two at 128 registers for every cluster shape.
 template <class S, int KIND, int CL>
-__global__ void __launch_bounds__(S::NT, (S::NT < (KIND == 1 ? 768 : 512)
-                                              ? (KIND == 1 ? 768 : 512) / S::NT
-                                              : 1))
+__global__ void __launch_bounds__(S::NT, (S::NT < 768 ? 768 / S::NT : 1))
     fwt_cluster_kernel(const PassParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   if constexpr (KIND == 1) {

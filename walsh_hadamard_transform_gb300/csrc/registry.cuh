@@ -319,12 +319,24 @@ KernelEntry col_entry() {
 template <class S, int KIND>
 cudaError_t launch_rowbits(const PassParams& p, long long tiles, int ncomp, cudaStream_t st) {
   const size_t smem = (size_t)(1u << S::TB) * (KIND == 1 || KIND == 3 ? 8 : 4);
-  fwt_rowbits_kernel<S, KIND><<<dim3((unsigned)tiles, (unsigned)ncomp), S::NT, smem, st>>>(p);
+  const dim3 grid((unsigned)tiles, (unsigned)ncomp);
+  if constexpr (has_bulk_row<S, KIND, false>()) {
+    if (p.bulk && (p.comp_elems & ((1ll << S::TB) - 1)) == 0) {
+      fwt_rowbits_bulk_kernel<S, KIND><<<grid, S::NT, smem, st>>>(p);
+      return cudaGetLastError();
+    }
+  }
+  fwt_rowbits_kernel<S, KIND><<<grid, S::NT, smem, st>>>(p);
   return cudaGetLastError();
 }
 template <class S, int KIND>
 cudaError_t setup_rowbits() {
   const size_t smem = (size_t)(1u << S::TB) * (KIND == 1 || KIND == 3 ? 8 : 4);
+  if constexpr (has_bulk_row<S, KIND, false>()) {
+    const cudaError_t err = cudaFuncSetAttribute(
+        fwt_rowbits_bulk_kernel<S, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+  }
   return cudaFuncSetAttribute(fwt_rowbits_kernel<S, KIND>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
 }
