@@ -109,6 +109,25 @@ int fwt_bits_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, in
                  int n, int64_t batch, int lo, int nbits, int normalize, fwt_stream_t stream);
 
 /*
+ * Transform on an arbitrary set of index bits (qubits): bit i of `mask` set means
+ * the butterfly stage of index bit i runs, i.e. y = (H or I per bit, Kronecker
+ * product) x, scaled by 2^{-popcount(mask)/2} when normalising ("[QDP] [feature]
+ * Pr4 kronecker fwt", deliverables: the factors (H_{n1} (x) I) and (I (x) H_{n2}) of
+ * the two-stage form, generalised to any subset of the factors H_2 of H_n).  mask
+ * must be below 2^n (else FWT_ERR_INVALID_ARG); 0 copies (scaled by 1).  A
+ * contiguous mask is the same call as fwt_bits_*.  Otherwise the set bits below
+ * 2^15 (2^14 for fp64) run in one pass over contiguous tiles with run-time
+ * butterfly masks, and each contiguous run above in strided column passes.  Other
+ * arguments, layout, in-place rules and errors as for fwt_batched_*.
+ */
+int fwt_mask_c32(const float* re_in, const float* im_in, float* re_out, float* im_out, int n,
+                 int64_t batch, uint32_t mask, int normalize, fwt_stream_t stream);
+int fwt_mask_c64(const double* re_in, const double* im_in, double* re_out, double* im_out, int n,
+                 int64_t batch, uint32_t mask, int normalize, fwt_stream_t stream);
+int fwt_mask_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, int32_t* im_out,
+                 int n, int64_t batch, uint32_t mask, int normalize, fwt_stream_t stream);
+
+/*
  * Diagonal phase, then transform (the IQP-encoding step: the state is multiplied
  * by a diagonal of phases before the Hadamard layer; "[QDP] [feature] Pr4
  * kronecker fwt", IQP shared-mem fused path):

@@ -148,6 +148,32 @@ class Oracle:
             raise RuntimeError(f"oracle_fwt_bits_f64 failed ({rc})")
         return out
 
+    def fwt_mask(self, x, mask: int, normalize: bool = True, nthreads: int = 1):
+        """Transform over the index bits set in ``mask``: the stages of those bits
+        commute, so this is the bit-range transform of each maximal run of set bits
+        in turn (the same butterfly loop, restricted to a run at a time), scaled by
+        2^{-popcount(mask)/2} in all when normalising."""
+        x = np.asarray(x)
+        n = self._n_of(x.shape[-1])
+        mask = int(mask)
+        if mask < 0 or mask >> n:
+            raise ValueError(f"mask {mask:#x} has bits at or above n = {n}")
+        runs, b = [], 0
+        while b < n:
+            if (mask >> b) & 1:
+                a = b
+                while b < n and (mask >> b) & 1:
+                    b += 1
+                runs.append((a, b - a))
+            else:
+                b += 1
+        y = x
+        for lo, k in runs:
+            y = self.fwt_bits(y, lo, k, normalize, nthreads)
+        if not runs:  # nothing transformed: a copy in the result type
+            y = self.fwt_bits(x, 0, 0, normalize, nthreads)
+        return y
+
     def fwt_complex(self, re, im, normalize: bool = True, nthreads: int = 1):
         """H is real, so a split complex vector transforms component by component."""
         out_im = None if im is None else self.fwt(im, normalize, nthreads)
@@ -215,6 +241,10 @@ def fwt_complex(re, im, normalize: bool = True, nthreads: int = 1):
 
 def fwt_bits(x, lo: int, nbits: int, normalize: bool = True, nthreads: int = 1) -> np.ndarray:
     return default().fwt_bits(x, lo, nbits, normalize, nthreads)
+
+
+def fwt_mask(x, mask: int, normalize: bool = True, nthreads: int = 1) -> np.ndarray:
+    return default().fwt_mask(x, mask, normalize, nthreads)
 
 
 def phase_fwt(re, im, theta, normalize: bool = True):

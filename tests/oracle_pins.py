@@ -259,6 +259,31 @@ def pin_phase_then_transform(orc):
         assert abs(a / e - 1) < 1e-14, "Parseval with phase"
 
 
+def pin_bit_mask(orc):
+    """The transform over an arbitrary set of index bits equals the dense Kronecker
+    product, index bit n-1 leftmost, of H_1 (the popc matrix of one bit) where the
+    bit is set and I_2 where it is not, scaled by 2^{-popcount/2}; for int32 the
+    same product modulo 2^32.  The empty set copies; the full set is the transform."""
+    rng = np.random.default_rng(31)
+    h1 = dense.hadamard_popc(1).astype(np.float64)
+    for n in (1, 4, 7, 9):
+        x = rng.standard_normal((2, 1 << n))
+        xi = rng.integers(-(2 ** 31), 2 ** 31, size=(2, 1 << n), dtype=np.int64).astype(np.int32)
+        masks = {0, (1 << n) - 1, 1, 1 << (n - 1)} | {int(m) for m in rng.integers(0, 1 << n, size=8)}
+        for mask in sorted(masks):
+            M = np.ones((1, 1))
+            for bit in reversed(range(n)):
+                M = np.kron(M, h1 if (mask >> bit) & 1 else np.eye(2))
+            k = bin(mask).count("1")
+            ref = x @ M.T * 2.0 ** (-k / 2.0)
+            assert _rel(orc.fwt_mask(x, mask, normalize=True), ref) < 1e-14, f"n={n} mask={mask:#x}"
+            refi = ((xi.astype(np.int64) @ M.T.astype(np.int64)) % (1 << 32)).astype(np.uint32).view(np.int32)
+            assert np.array_equal(orc.fwt_mask(xi, mask, normalize=False), refi), f"int n={n} mask={mask:#x}"
+    x = rng.standard_normal((1, 1 << 12))
+    assert _rel(orc.fwt_mask(x, (1 << 12) - 1), orc.fwt(x)) < 1e-15
+    assert np.array_equal(orc.fwt_mask(x, 0, normalize=True), x)
+
+
 ORACLE_PINS = [
     pin_butterfly_vs_dense_float,
     pin_butterfly_vs_dense_int,
@@ -272,5 +297,6 @@ ORACLE_PINS = [
     pin_scale,
     pin_fp32_promotion,
     pin_bit_range,
+    pin_bit_mask,
     pin_phase_then_transform,
 ]

@@ -233,3 +233,16 @@ def test_host_workspace_size(lib):
     assert ws(fwt.FWT_I32, 12, 1 << 16, with_im=False) == 3 * 4096 * (4 << 12)
     assert ws(fwt.FWT_I32, 12, 1 << 14, with_im=False) == 3 * 2048 * (4 << 12)
     assert ws(fwt.FWT_C32, 4, 0) == 0 and ws(fwt.FWT_C32, 31, 1) == 0 and ws(7, 4, 1) == 0
+
+
+@pytest.mark.parametrize("fn", ["fwt_mask_c32", "fwt_mask_c64", "fwt_mask_i32"])
+def test_mask_argument_errors_before_launch(lib, fn):
+    f = getattr(fwt, fn)
+    norm = 0 if fn.endswith("i32") else 1
+    a, b, c, d = A, A + GiB, A + 2 * GiB, A + 3 * GiB
+    assert f(a, b, c, d, 4, 1, 1 << 4, norm, None) == fwt.FWT_ERR_INVALID_ARG  # bit 4 of n = 4
+    assert f(a, b, c, d, -1, 1, 0, norm, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, c, d, 31, 1, 1, norm, None) == fwt.FWT_ERR_INVALID_ARG
+    assert f(None, None, None, None, 4, 0, 0b101, norm, None) == fwt.FWT_OK  # empty batch
+    assert f(a + 4, b, c, d, 4, 1, 0b101, norm, None) == fwt.FWT_ERR_MISALIGNED
+    assert f(a, b, a + 16, d, 4, 1, 0b101, norm, None) == fwt.FWT_ERR_INVALID_ARG

@@ -74,3 +74,51 @@ def test_bit_range_argument_errors():
     assert fwt.fwt_bits_c32(*p, 5, 1, 2, -1, 1, None) == fwt.FWT_ERR_INVALID_ARG
     assert fwt.fwt_bits_c32(*p, 5, 1, 1, 4, 1, None) == fwt.FWT_OK
     torch.cuda.synchronize()
+
+
+def _gpu_mask(re, im, mask, norm, inplace=False):
+    dre, dim_ = torch.from_numpy(re).cuda(), torch.from_numpy(im).cuda()
+    if inplace:
+        fwt.transform(dre, dim_, dre, dim_, normalize=norm, mask=mask)
+        out = (dre, dim_)
+    else:
+        out = fwt.transform(dre, dim_, normalize=norm, mask=mask)
+    torch.cuda.synchronize()
+    return out[0].cpu().numpy(), out[1].cpu().numpy()
+
+
+def _masks(n, rmax):
+    full = (1 << n) - 1
+    m = {0, full, 1, 1 << (n - 1), full & 0x5555_5555, full & 0xAAAA_AAAA}
+    if n >= 6:
+        m |= {0b101101, (1 << (n - 1)) | 1, full & ~(1 << (n // 2))}
+    if n > rmax:  # runs above the row tiles, and one crossing their limit
+        m |= {(1 << rmax) | 0b110, (0b11 << (rmax - 1)) | (1 << (n - 1)),
+              full & ~((1 << rmax) - 1) & ~(1 << (rmax + 2)) | 0b1001}
+    return sorted(x & full for x in m)
+
+
+@pytest.mark.parametrize("dtype", ["c32", "c64", "i32"])
+@pytest.mark.parametrize("n", [3, 9, 13, 17, 21])
+def test_bit_masks_match_oracle(dtype, n):
+    """Any set of index bits: the set bits within the row tiles in one run-time-mask
+    pass, runs above them in column passes; against the oracle's composition of
+    bit ranges, in and out of place."""
+    rmax = 14 if dtype == "c64" else 15
+    batch = 3 if n < 20 else 1
+    norm_opts = (False,) if dtype == "i32" else (True, False)
+    re, im = inputs.random_pair(n, batch, dtype, seed=40 + n)
+    for i, mask in enumerate(_masks(n, rmax)):
+        for norm in norm_opts:
+            gre, gim = _gpu_mask(re, im, mask, norm, inplace=(i % 2 == 1))
+            ore = oracle.fwt_mask(re, mask, normalize=norm, nthreads=4)
+            oim = oracle.fwt_mask(im, mask, normalize=norm, nthreads=4)
+            assert_matches(dtype, gre, gim, ore, oim, f"{dtype} n={n} mask={mask:#x} norm={norm}")
+
+
+def test_bit_mask_argument_errors():
+    a = torch.zeros(2, 1 << 5, device="cuda")
+    with pytest.raises(fwt.FwtError):
+        fwt.transform(a, a.clone(), mask=1 << 5)
+    with pytest.raises(ValueError):
+        fwt.transform(a, a.clone(), mask=1, bits=(0, 1))

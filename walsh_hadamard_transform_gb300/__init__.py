@@ -58,6 +58,10 @@ def library() -> ctypes.CDLL:
             f = getattr(lib, name)
             f.argtypes = [vp, vp, vp, vp, ci, i64, ci, ci, ci, vp]
             f.restype = ci
+        for name in ("fwt_mask_c32", "fwt_mask_c64", "fwt_mask_i32"):
+            f = getattr(lib, name)
+            f.argtypes = [vp, vp, vp, vp, ci, i64, ctypes.c_uint32, ci, vp]
+            f.restype = ci
         lib.fwt_phase_c32.argtypes = [vp, vp, vp, i64, vp, vp, ci, i64, ci, vp]
         lib.fwt_phase_c32.restype = ci
         for name in ("fwt_host_c32", "fwt_host_c64", "fwt_host_i32"):
@@ -141,6 +145,21 @@ def fwt_bits_c64(re_in, im_in, re_out, im_out, n, batch, lo, nbits, normalize, s
 def fwt_bits_i32(re_in, im_in, re_out, im_out, n, batch, lo, nbits, normalize, stream) -> int:
     return library().fwt_bits_i32(re_in, im_in, re_out, im_out, n, batch, lo, nbits,
                                   int(normalize), stream)
+
+
+def fwt_mask_c32(re_in, im_in, re_out, im_out, n, batch, mask, normalize, stream) -> int:
+    return library().fwt_mask_c32(re_in, im_in, re_out, im_out, n, batch, mask, int(normalize),
+                                  stream)
+
+
+def fwt_mask_c64(re_in, im_in, re_out, im_out, n, batch, mask, normalize, stream) -> int:
+    return library().fwt_mask_c64(re_in, im_in, re_out, im_out, n, batch, mask, int(normalize),
+                                  stream)
+
+
+def fwt_mask_i32(re_in, im_in, re_out, im_out, n, batch, mask, normalize, stream) -> int:
+    return library().fwt_mask_i32(re_in, im_in, re_out, im_out, n, batch, mask, int(normalize),
+                                  stream)
 
 
 def fwt_phase_c32(re_in, im_in, theta, theta_stride, re_out, im_out, n, batch, normalize,
@@ -365,6 +384,7 @@ class PassTrace:
 _ENTRY = {"c32": fwt_batched_c32, "c64": fwt_batched_c64, "i32": fwt_batched_i32}
 _BITS_ENTRY = {"c32": fwt_bits_c32, "c64": fwt_bits_c64, "i32": fwt_bits_i32}
 _HOST_ENTRY = {"c32": fwt_host_c32, "c64": fwt_host_c64, "i32": fwt_host_i32}
+_MASK_ENTRY = {"c32": fwt_mask_c32, "c64": fwt_mask_c64, "i32": fwt_mask_i32}
 
 
 def _dtype_key(t) -> str:
@@ -377,14 +397,15 @@ def _dtype_key(t) -> str:
 
 
 def transform(re, im=None, out_re=None, out_im=None, normalize: bool = True, stream=None,
-              bits=None):
+              bits=None, mask=None):
     """Transform the rows of ``re`` / ``im`` (CUDA tensors of shape (batch, 2^n)).
 
     Outputs are new tensors unless ``out_re`` / ``out_im`` are given (they may be
     the inputs themselves, for an in-place transform).  ``im`` may be None only
     for int32 (real-only input).  Runs on ``stream`` (default: the current
     PyTorch stream); the call does not synchronise.  ``bits=(lo, nbits)``
-    transforms index bits [lo, lo + nbits) only (I (x) H_nbits (x) I).  Returns
+    transforms index bits [lo, lo + nbits) only (I (x) H_nbits (x) I); ``mask``
+    (an int below 2^n) transforms the index bits set in it.  Returns
     (out_re, out_im).
     """
     import torch
@@ -415,12 +436,17 @@ def transform(re, im=None, out_re=None, out_im=None, normalize: bool = True, str
     ptrs = (re.data_ptr(), im.data_ptr() if im is not None else None, out_re.data_ptr(),
             out_im.data_ptr() if out_im is not None else None)
     with torch.cuda.device(re.device):
-        if bits is None:
+        if bits is not None and mask is not None:
+            raise ValueError("give bits or mask, not both")
+        if mask is not None:
+            st = _MASK_ENTRY[key](*ptrs, n, batch, int(mask), normalize, handle)
+        elif bits is None:
             st = _ENTRY[key](*ptrs, n, batch, normalize, handle)
         else:
             st = _BITS_ENTRY[key](*ptrs, n, batch, int(bits[0]), int(bits[1]), normalize, handle)
     if st != FWT_OK:
-        what = f"fwt_batched_{key}" if bits is None else f"fwt_bits_{key}(bits={tuple(bits)})"
+        what = (f"fwt_mask_{key}(mask={mask:#x})" if mask is not None else
+                f"fwt_batched_{key}" if bits is None else f"fwt_bits_{key}(bits={tuple(bits)})")
         raise FwtError(st, f"{what}(n={n}, batch={batch})")
     return out_re, out_im
 

@@ -294,6 +294,7 @@ struct PassSpec {
   int L;        // column passes: log2 of the row stride
   int bits_lo;  // run-time bit-range row passes: first transformed tile bit
   int bits_k;   //   ... and how many
+  uint32_t mask = 0;  // run-time row passes over a set of tile bits instead
 };
 
 // The column pass over bits [L, L + K): the plan's segment width when a tile
@@ -334,6 +335,17 @@ bool column_passes(int dtype, int L, int hi, const Plan& plan, std::vector<PassS
 }
 
 // Passes of the whole transform for a Kronecker plan (factor 0 = row pass).
+// The kernel of a row pass over the low K bits.  fp64 row tiles of 2^14 elements
+// run on a CTA pair (three CTAs an SM) rather than as one 512-thread CTA holding the
+// whole tile, unless cluster kernels are off.
+const KernelEntry* row_kernel(int dtype, int K) {
+  if (dtype == FWT_C64 && K == 14 && cluster_mode() > 0) {
+    const KernelEntry* c = find_kernel(dtype, KIND_CLUSTER, 14, 13);
+    if (c && cluster_runnable(c)) return c;
+  }
+  return find_kernel(dtype, K <= 2 ? KIND_SMALL : KIND_ROW, K);
+}
+
 bool full_passes(int n, int dtype, const Plan& plan, std::vector<PassSpec>& out) {
   if (plan.cluster) {
     out.push_back(PassSpec{plan.cluster, 0, 0, 0});
@@ -343,14 +355,7 @@ bool full_passes(int n, int dtype, const Plan& plan, std::vector<PassSpec>& out)
   for (int f = 0; f < plan.nf; ++f) {
     const int K = plan.bits[f];
     PassSpec ps{nullptr, L, 0, 0};
-    if (f == 0 && dtype == FWT_C64 && K == 14 && cluster_mode() > 0) {
-      // fp64 row tiles of 2^14 elements: a CTA pair (three CTAs an SM) instead of
-      // one 512-thread CTA holding the whole tile
-      const KernelEntry* c = find_kernel(dtype, KIND_CLUSTER, 14, 13);
-      if (c && cluster_runnable(c)) ps.e = c;
-    }
-    if (ps.e) {  // chosen above
-    } else if (f == 0) ps.e = find_kernel(dtype, K <= 2 ? KIND_SMALL : KIND_ROW, K);
+    if (f == 0) ps.e = row_kernel(dtype, K);
     else ps.e = find_kernel(dtype, KIND_COL, K, plan.col_bytes, col_tma(plan, K));
     if (!ps.e) return false;
     out.push_back(ps);
@@ -394,6 +399,36 @@ bool range_passes(int n, int dtype, int lo, int k, const Plan& plan, std::vector
   return top == hi || column_passes(dtype, top, hi, plan, out);
 }
 
+// Passes of the transform over an arbitrary set of index bits (`mask`, below 2^n).
+// One contiguous run is a bit range.  Otherwise the bits below the row-tile limit
+// go to one run-time-mask row pass (tiles of 2^12 .. 2^rmax elements), and every
+// run above it to column passes at its own stride.
+bool mask_passes(int n, int dtype, uint32_t mask, const Plan& plan, std::vector<PassSpec>& out) {
+  if (mask == 0) return range_passes(n, dtype, 0, 0, plan, out);
+  const int lo = __builtin_ctz(mask), hi = 32 - __builtin_clz(mask);
+  if (mask == (((hi >= 32 ? 0u : (1u << hi)) - 1u) & ~((1u << lo) - 1u)))
+    return range_passes(n, dtype, lo, hi - lo, plan, out);
+  const int rmax = max_row_bits(dtype);
+  const uint32_t low = rmax >= 32 ? mask : mask & ((1u << rmax) - 1u);
+  if (low) {
+    const int top = 32 - __builtin_clz(low);
+    const KernelEntry* e = find_kernel(dtype, KIND_ROWBITS, std::min(std::max(top, 12), rmax));
+    if (!e) return false;
+    PassSpec ps{e, 0, 0, 0};
+    ps.mask = low;
+    out.push_back(ps);
+  }
+  uint32_t high = mask & ~low;
+  while (high) {  // each run [a, b) above the row tiles
+    const int a = __builtin_ctz(high);
+    int b = a;
+    while (b < 32 && ((high >> b) & 1u)) ++b;
+    if (!column_passes(dtype, a, b, plan, out)) return false;
+    high &= b >= 32 ? 0u : ~((1u << b) - 1u);
+  }
+  return true;
+}
+
 int check_arrays(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out,
                  int n, int64_t batch, bool& has_im) {
   const int esz = elem_size(dtype);
@@ -421,8 +456,9 @@ int check_arrays(int dtype, const void* re_in, const void* im_in, void* re_out, 
 // Runs the transform over bits [lo, lo + k) of each vector (the whole transform
 // when lo = 0, k = n), scaled by 2^{-k/2} when normalising.
 int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out, int n,
-        int64_t batch, int lo, int k, int normalize, cudaStream_t stream) {
+        int64_t batch, int lo, int k, int normalize, cudaStream_t stream, uint32_t mask = 0) {
   if (n < 0 || n > 30 || batch < 0 || lo < 0 || k < 0 || lo + k > n) return FWT_ERR_INVALID_ARG;
+  if (mask && (n < 32 && (mask >> n) != 0)) return FWT_ERR_INVALID_ARG;
   if (dtype == FWT_I32 && normalize) return FWT_ERR_UNSUPPORTED;
   if (batch == 0) return FWT_OK;
   bool has_im = false;
@@ -439,7 +475,12 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
   if (whole && !plan.cluster && !plan_valid(n, dtype, plan)) return FWT_ERR_UNSUPPORTED;
   if (plan.tma && !tensor_map_encoder()) plan.tma = 0;  // driver without the TMA encoder
   std::vector<PassSpec> passes;
-  if (!range_passes(n, dtype, lo, k, plan, passes)) return FWT_ERR_UNSUPPORTED;
+  if (mask) {
+    if (!mask_passes(n, dtype, mask, plan, passes)) return FWT_ERR_UNSUPPORTED;
+    k = __builtin_popcount(mask);  // the normalisation counts the transformed bits
+  } else if (!range_passes(n, dtype, lo, k, plan, passes)) {
+    return FWT_ERR_UNSUPPORTED;
+  }
 
   PassParams p{};
   const double s = k % 2 == 0 ? std::ldexp(1.0, -k / 2) : std::ldexp(1.0, -(k - 1) / 2) / std::sqrt(2.0);
@@ -506,6 +547,7 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
         p.stride_log = ps.L;
         p.bits_lo = ps.bits_lo;
         p.bits_k = ps.bits_k;
+        p.bits_mask = ps.mask;
         const bool last = f == npass - 1;
         p.do_scale = (normalize && last) ? 1 : 0;
         p.ld_policy = 1;                             // read once
@@ -643,6 +685,26 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace fwt
 
+namespace fwt {
+namespace {
+// A set of bits: one contiguous run goes the bit-range way (the whole transform
+// included), anything else through mask_passes.
+int run_mask(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out, int n,
+             int64_t batch, uint32_t mask, int normalize, fwt_stream_t stream) {
+  if (n < 0 || n > 30) return FWT_ERR_INVALID_ARG;
+  if ((mask >> n) != 0) return FWT_ERR_INVALID_ARG;
+  if (mask != 0) {  // one contiguous run is a bit range (the whole transform included)
+    const int lo = __builtin_ctz(mask), hi = 32 - __builtin_clz(mask);
+    if (mask == (((hi >= 32 ? 0u : (1u << hi)) - 1u) & ~((1u << lo) - 1u)))
+      return run(dtype, re_in, im_in, re_out, im_out, n, batch, lo, hi - lo, normalize,
+                      (cudaStream_t)stream);
+  }
+  return run(dtype, re_in, im_in, re_out, im_out, n, batch, 0, 0, normalize,
+                  (cudaStream_t)stream, mask);
+}
+}  // namespace
+}  // namespace fwt
+
 extern "C" {
 
 int fwt_batched_c32(const float* re_in, const float* im_in, float* re_out, float* im_out, int n,
@@ -682,6 +744,21 @@ int fwt_bits_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, in
                  int n, int64_t batch, int lo, int nbits, int normalize, fwt_stream_t stream) {
   return fwt::run(FWT_I32, re_in, im_in, re_out, im_out, n, batch, lo, nbits, normalize,
                   (cudaStream_t)stream);
+}
+
+int fwt_mask_c32(const float* re_in, const float* im_in, float* re_out, float* im_out, int n,
+                 int64_t batch, uint32_t mask, int normalize, fwt_stream_t stream) {
+  return fwt::run_mask(FWT_C32, re_in, im_in, re_out, im_out, n, batch, mask, normalize, stream);
+}
+
+int fwt_mask_c64(const double* re_in, const double* im_in, double* re_out, double* im_out, int n,
+                 int64_t batch, uint32_t mask, int normalize, fwt_stream_t stream) {
+  return fwt::run_mask(FWT_C64, re_in, im_in, re_out, im_out, n, batch, mask, normalize, stream);
+}
+
+int fwt_mask_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, int32_t* im_out,
+                 int n, int64_t batch, uint32_t mask, int normalize, fwt_stream_t stream) {
+  return fwt::run_mask(FWT_I32, re_in, im_in, re_out, im_out, n, batch, mask, normalize, stream);
 }
 
 int fwt_phase_c32(const float* re_in, const float* im_in, const float* theta,

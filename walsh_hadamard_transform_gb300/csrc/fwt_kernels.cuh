@@ -51,6 +51,7 @@ struct PassParams {
   int ld_policy;         // L2 eviction priority of the loads: 0 normal, 1 first, 2 last
   int st_policy;         // ... and of the stores
   int bits_lo, bits_k;   // run-time bit-range tiles: transformed tile bits [lo, lo + k)
+  uint32_t bits_mask;    // ... or, when non-zero, this set of tile bits
   const float* theta;    // phase pass: angles, theta[b * theta_stride + i]
   long long theta_stride;
   int n;                 // phase pass: log2 of the vector length
@@ -357,11 +358,12 @@ struct RuntimeBits {
   static constexpr bool kMayTruncate = true;  // decided at run time from tk
   __device__ explicit RuntimeBits(const PassParams& p) {
     uint32_t rm[3];
-    S::round_masks(p.bits_lo, p.bits_k, rm);
+    if (p.bits_mask) S::round_masks_set(p.bits_mask, rm);
+    else S::round_masks(p.bits_lo, p.bits_k, rm);
     r1 = rm[0];
     r2 = rm[1];
     r3 = rm[2];
-    tk = p.bits_k;
+    tk = p.bits_mask ? __popc(p.bits_mask) : p.bits_k;
   }
 };
 

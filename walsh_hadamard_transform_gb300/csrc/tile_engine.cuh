@@ -95,7 +95,11 @@ struct Shape {
   // The same three register masks for transformed tile bits [ts, ts+tk) given at
   // run time (a transform on a sub-range of the index bits).
   __host__ __device__ static constexpr void round_masks(int ts, int tk, uint32_t (&rm)[3]) {
-    const uint32_t tset = (tk <= 0 ? 0u : ((tk >= 32 ? 0u : (1u << tk)) - 1u)) << ts;
+    round_masks_set((tk <= 0 ? 0u : ((tk >= 32 ? 0u : (1u << tk)) - 1u)) << ts, rm);
+  }
+  // ... and for any set of tile bits (a bit mask below 2^TB): the three layouts'
+  // register bits cover every tile bit, so any set is partitioned among the rounds.
+  __host__ __device__ static constexpr void round_masks_set(uint32_t tset, uint32_t (&rm)[3]) {
     const uint32_t d1 = reg_elem_bits(1) & tset;
     const uint32_t d2 = reg_elem_bits(2) & tset & ~d1;
     const uint32_t d3 = reg_elem_bits(3) & tset & ~(d1 | d2);
