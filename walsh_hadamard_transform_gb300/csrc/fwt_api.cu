@@ -112,24 +112,40 @@ bool plan_valid(int n, int dtype, const Plan& p) {
   return sum == n;
 }
 
-// Splits measured faster than the general rule for large vectors (GB300, a sweep
-// of every split and column width at 2^28 elements a part).  4-byte types: at
-// n = 25, 26 a 32-byte column factor of 11 bits; from n = 27 three passes with
-// 128-byte column segments (each pass near 7 TB/s) beat two passes that need
-// narrow segments.  fp64: tiles of 2^14 elements run one 512-thread CTA an SM and
-// reach about half the rate of the 2^13-element tiles (three CTAs an SM), so from
-// n = 26 three passes over tiles of at most 2^13 elements win.
-struct LargeSplit {
+// Splits measured faster than the general rule (GB300, a sweep of every two-factor
+// split, column width and TMA mode at 2^26 elements a part for n <= 23, of every
+// split and width at 2^28 for larger n).
+//  * fp64 n = 15..23: a row factor of 9..12 bits and a column factor of 6..11 at 64-
+//    or 128-byte segments, every column tile staged by TMA (the TMA column kernel
+//    runs three CTAs an SM; the direct one two): passes of few bits are HBM-bound
+//    (~6.7 TB/s), 15-25% faster than the general rule.
+//  * 4-byte n = 18..22: 128-byte column segments (3-4% faster).
+//  * 4-byte n = 25, 26: an 11-bit column factor at 32 bytes; from n = 27 three
+//    passes with 128-byte column segments (each near 7 TB/s) beat two passes that
+//    need narrow segments.
+//  * fp64 from n = 25: tiles of 2^14 elements run one 512-thread CTA (or a CTA pair)
+//    at about half the rate of the 2^13-element tiles, so from n = 26 three passes
+//    over tiles of at most 2^13 elements win.
+struct MeasuredSplit {
   bool fp64;
   int n, nf, bits[3], col_bytes;
+  bool tma_always;  // every column factor TMA-staged (when the TMA mode is auto)
 };
-constexpr LargeSplit kLargeSplits[] = {
-    {false, 25, 2, {14, 11, 0}, 32}, {false, 26, 2, {15, 11, 0}, 32},
-    {false, 27, 3, {12, 7, 8}, 128}, {false, 28, 3, {13, 8, 7}, 128},
-    {false, 29, 3, {13, 8, 8}, 128}, {false, 30, 3, {14, 8, 8}, 128},
-    {true, 25, 2, {14, 11, 0}, 32},  {true, 26, 3, {12, 6, 8}, 128},
-    {true, 27, 3, {12, 7, 8}, 128},  {true, 28, 3, {12, 8, 8}, 128},
-    {true, 29, 3, {12, 10, 7}, 64},  {true, 30, 3, {13, 10, 7}, 64},
+constexpr MeasuredSplit kMeasuredSplits[] = {
+    {true, 15, 2, {9, 6, 0}, 128, true},    {true, 16, 2, {10, 6, 0}, 128, true},
+    {true, 17, 2, {10, 7, 0}, 128, true},   {true, 18, 2, {10, 8, 0}, 128, true},
+    {true, 19, 2, {12, 7, 0}, 128, true},   {true, 20, 2, {12, 8, 0}, 128, true},
+    {true, 21, 2, {11, 10, 0}, 64, true},   {true, 22, 2, {12, 10, 0}, 64, true},
+    {true, 23, 2, {12, 11, 0}, 32, false},
+    {false, 18, 2, {12, 6, 0}, 128, false}, {false, 19, 2, {13, 6, 0}, 128, false},
+    {false, 20, 2, {13, 7, 0}, 128, false}, {false, 21, 2, {13, 8, 0}, 128, false},
+    {false, 22, 2, {14, 8, 0}, 128, false},
+    {false, 25, 2, {14, 11, 0}, 32, false}, {false, 26, 2, {15, 11, 0}, 32, false},
+    {false, 27, 3, {12, 7, 8}, 128, false}, {false, 28, 3, {13, 8, 7}, 128, false},
+    {false, 29, 3, {13, 8, 8}, 128, false}, {false, 30, 3, {14, 8, 8}, 128, false},
+    {true, 25, 2, {14, 11, 0}, 32, false},  {true, 26, 3, {12, 6, 8}, 128, false},
+    {true, 27, 3, {12, 7, 8}, 128, false},  {true, 28, 3, {12, 8, 8}, 128, false},
+    {true, 29, 3, {12, 10, 7}, 64, false},  {true, 30, 3, {13, 10, 7}, 64, false},
 };
 
 Plan default_plan(int n, int dtype) {
@@ -142,12 +158,13 @@ Plan default_plan(int n, int dtype) {
   }
   p.col_bytes = width ? width : default_col_bytes(dtype);
   if (width == 0) {
-    for (const LargeSplit& ls : kLargeSplits) {
-      if (ls.fp64 != (dtype == FWT_C64) || ls.n != n) continue;
+    for (const MeasuredSplit& ms : kMeasuredSplits) {
+      if (ms.fp64 != (dtype == FWT_C64) || ms.n != n) continue;
       Plan q = p;
-      q.nf = ls.nf;
-      for (int f = 0; f < 3; ++f) q.bits[f] = ls.bits[f];
-      q.col_bytes = ls.col_bytes;
+      q.nf = ms.nf;
+      for (int f = 0; f < 3; ++f) q.bits[f] = ms.bits[f];
+      q.col_bytes = ms.col_bytes;
+      if (ms.tma_always && q.tma == 1) q.tma = 2;
       if (plan_valid(n, dtype, q)) return q;
     }
   }

@@ -409,7 +409,8 @@ __device__ __forceinline__ unsigned long long shr64(unsigned long long v, uint32
 //   TO_FIXED_TRUNC: F <= 51 and emax >= F + 12, so a zero or subnormal element would
 //                   shift right by 64 bits or more whatever its leading bit: every
 //                   element is taken as a normal number, and the magnitude is
-//                   truncated (error below one unit instead of half a unit).
+//                   truncated (error below one unit instead of half a unit, and of
+//                   either sign, so the errors of a tile carry no common bias).
 enum ToFixedMode { TO_FIXED_ANY, TO_FIXED_ROUND, TO_FIXED_TRUNC };
 template <int MODE>
 __device__ __forceinline__ long long to_fixed(long long bits, int emax, int F) {
