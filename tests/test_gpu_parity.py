@@ -386,3 +386,13 @@ def test_fp64_cluster_pairs():
     gre, gim = gpu_transform(wide, wide[::-1].copy(), True)
     ore, oim = oracle.fwt_complex(wide, wide[::-1].copy(), normalize=True)
     assert_matches("c64", gre, gim, ore, oim, "cluster pair, wide dynamic range")
+
+
+@pytest.mark.parametrize("dtype", ["c32", "c64", "i32"])
+@pytest.mark.parametrize("n", [21, 22, 23, 25])
+def test_default_plans_mid_and_large_n(dtype, n):
+    """The measured default plans between the every-n range and the benchmark size
+    (fp64: TMA-staged column tiles of 64/128-byte segments; 4-byte: 128-byte
+    segments; n = 25: 32-byte 11-bit column factors), in and out of place."""
+    for inplace in (False, True):
+        _check(dtype, n, 1, dtype != "i32", seed=200 + n, inplace=inplace)
