@@ -569,7 +569,7 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
         p.do_scale = (normalize && last) ? 1 : 0;
         p.ld_policy = 1;                             // read once
         p.st_policy = last ? 1 : (chunked ? 2 : 0);  // keep intermediates for the next pass
-        p.bulk = g_use_tma != 0 ? 1 : 0;             // bulk-copied fp64 row tiles
+        p.bulk = plan.tma != 0 ? 1 : 0;              // bulk-copied fp64 row tiles
         const bool traced = g_trace_count + 2 <= g_trace_capacity;
         if (traced) {
           err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count], stream);
