@@ -396,3 +396,41 @@ def test_default_plans_mid_and_large_n(dtype, n):
     segments; n = 25: 32-byte 11-bit column factors), in and out of place."""
     for inplace in (False, True):
         _check(dtype, n, 1, dtype != "i32", seed=200 + n, inplace=inplace)
+
+
+def test_concurrent_host_threads():
+    """Two host threads issuing transforms on their own streams at the same time
+    (settings and plans under locks, tracing per thread) give the single-threaded
+    results exactly (same plan, same kernels: deterministic)."""
+    import threading
+
+    cases = [("c32", 18, 4), ("c64", 16, 4), ("i32", 20, 2), ("c64", 22, 1)]
+    data, expect = [], []
+    for i, (dtype, n, batch) in enumerate(cases):
+        re, im = inputs.random_pair(n, batch, dtype, seed=300 + i)
+        a, b = torch.from_numpy(re).cuda(), torch.from_numpy(im).cuda()
+        data.append((dtype, a, b))
+        expect.append(fwt.transform(a, b, normalize=dtype != "i32"))
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(idx):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(10):
+                    for k in range(idx, len(data), 2):
+                        dtype, a, b = data[k]
+                        out = fwt.transform(a, b, normalize=dtype != "i32")
+                        s.synchronize()
+                        if not (torch.equal(out[0], expect[k][0]) and torch.equal(out[1], expect[k][1])):
+                            errors.append((idx, k))
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
