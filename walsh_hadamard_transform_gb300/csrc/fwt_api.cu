@@ -236,7 +236,17 @@ Plan get_plan(int n, int dtype) {
 std::mutex g_dev_mu;
 std::vector<char> g_dev_ready;
 std::vector<long long> g_dev_l2;  // L2 bytes per device
+std::vector<int> g_dev_sms;       // SMs per device
 long long g_chunk_bytes = 0;       // -1: half the L2 of the current device; 0: off (default)
+
+// Tiles one wave of the three-CTA-an-SM staged kernels covers: how far ahead their
+// L2 prefetch reaches (the tile that starts on a CTA slot when the current one ends).
+int prefetch_ahead() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  return dev < (int)g_dev_sms.size() ? 3 * g_dev_sms[dev] : 0;
+}
 
 long long chunk_budget() {
   int dev = 0;
@@ -262,6 +272,11 @@ cudaError_t ensure_device() {
   if (err != cudaSuccess) return err;
   if ((int)g_dev_l2.size() <= dev) g_dev_l2.resize(dev + 1, 0);
   g_dev_l2[dev] = l2;
+  int sms = 0;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  if ((int)g_dev_sms.size() <= dev) g_dev_sms.resize(dev + 1, 0);
+  g_dev_sms[dev] = sms;
   g_dev_ready[dev] = 1;
   return cudaSuccess;
 }
@@ -500,6 +515,7 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
   }
 
   PassParams p{};
+  const int ahead = prefetch_ahead();
   const double s = k % 2 == 0 ? std::ldexp(1.0, -k / 2) : std::ldexp(1.0, -(k - 1) / 2) / std::sqrt(2.0);
   p.scale_f64 = s;
   p.scale_f32 = (float)s;
@@ -570,6 +586,7 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
         p.ld_policy = 1;                             // read once
         p.st_policy = last ? 1 : (chunked ? 2 : 0);  // keep intermediates for the next pass
         p.bulk = plan.tma != 0 ? 1 : 0;              // bulk-copied fp64 row tiles
+        p.prefetch_ahead = ahead;
         const bool traced = g_trace_count + 2 <= g_trace_capacity;
         if (traced) {
           err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count], stream);

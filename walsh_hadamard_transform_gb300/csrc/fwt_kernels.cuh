@@ -52,6 +52,7 @@ struct PassParams {
   int st_policy;         // ... and of the stores
   int bits_lo, bits_k;   // run-time bit-range tiles: transformed tile bits [lo, lo + k)
   uint32_t bits_mask;    // ... or, when non-zero, this set of tile bits
+  int prefetch_ahead;    // staged tiles: also prefetch into L2 the tile this many ahead (0: off)
   const float* theta;    // phase pass: angles, theta[b * theta_stride + i]
   long long theta_stride;
   int n;                 // phase pass: log2 of the vector length
@@ -231,13 +232,15 @@ __device__ __forceinline__ bool wait_tile(uint64_t* bar) {
 
 // TMA: the column tile arrives in shared memory in natural order; threads pick up
 // layout L1 there, and write layout L3 back there for a TMA store.
-template <class S>
+template <class S, int ESZ>
 struct TmaMover {
+  static constexpr bool kPrefetch = (ESZ << S::TS) >= 128;  // segments of 128+ bytes
   static constexpr int BOXR = S::TK >= 8 ? 256 : (1 << S::TK);  // rows per copy
   static constexpr int NBOX = (1 << S::TK) / BOXR;
   static constexpr uint32_t BOX_ELEMS = (uint32_t)BOXR << S::TS;
   const CUtensorMap* map;
   int col0, row0;
+  int pf_col = -1, pf_row = 0;  // tile to prefetch into L2 (none: pf_col < 0)
   unsigned char* smem;
   uint64_t* bar;
   __device__ TmaMover(const TmaPassParams& tp, unsigned char* smem_raw, uint64_t* barrier) {
@@ -247,6 +250,13 @@ struct TmaMover {
     const long long tile = blockIdx.x;
     col0 = (int)((tile & ((1ll << chunks_lg) - 1)) << S::TS);
     row0 = (int)((tile >> chunks_lg) << S::TK);
+    // Wide segments (128 bytes and more) prefetch, one wave ahead, the tile that will
+    // start on this CTA slot next (measured 5% faster); narrower ones measured slower.
+    const long long next = tile + tp.p.prefetch_ahead;
+    if (kPrefetch && tp.p.prefetch_ahead > 0 && next < (long long)gridDim.x) {
+      pf_col = (int)((next & ((1ll << chunks_lg) - 1)) << S::TS);
+      pf_row = (int)((next >> chunks_lg) << S::TK);
+    }
     smem = smem_raw;
     bar = barrier;
     if (threadIdx.x == 0) mbar_init(bar, 1);
@@ -260,6 +270,10 @@ struct TmaMover {
 #pragma unroll
       for (int i = 0; i < NBOX; ++i)
         tma_load_2d(smem + (size_t)i * BOX_ELEMS * sizeof(U), map, col0, row0 + i * BOXR, bar, pol);
+      if (pf_col >= 0) {
+#pragma unroll
+        for (int i = 0; i < NBOX; ++i) tma_prefetch_2d(map, pf_col, pf_row + i * BOXR);
+      }
     }
     if (!wait_tile(bar)) return false;  // the whole tile is skipped
     const U* sm = reinterpret_cast<const U*>(smem);
@@ -294,10 +308,16 @@ template <class S>
 struct BulkMover {
   const char* src;
   char* dst;
+  int prefetch;  // tiles ahead to prefetch into L2 (0: none)
   unsigned char* smem;
   uint64_t* bar;
   __device__ BulkMover(const PassParams& p, unsigned char* smem_raw, uint64_t* barrier) {
     const bool im = blockIdx.y != 0;
+    // prefetch into L2, one wave ahead, the tile that will start on this CTA slot
+    // next (measured 3-5% faster)
+    prefetch = p.prefetch_ahead > 0 && (long long)blockIdx.x + p.prefetch_ahead < (long long)gridDim.x
+                   ? p.prefetch_ahead
+                   : 0;
     src = static_cast<const char*>(im ? p.in[1] : p.in[0]);
     dst = static_cast<char*>(im ? p.out[1] : p.out[0]);
     smem = smem_raw;
@@ -315,6 +335,11 @@ struct BulkMover {
       mbar_arrive_expect_tx(bar, BYTES);
 #pragma unroll
       for (uint32_t o = 0; o < BYTES; o += CH) bulk_load(smem + o, g + o, CH, bar, pol);
+      if (prefetch) {
+        const char* nxt = g + (size_t)prefetch * BYTES;
+#pragma unroll
+        for (uint32_t o = 0; o < BYTES; o += CH) bulk_prefetch(nxt + o, CH);
+      }
     }
     if (!wait_tile(bar)) return false;  // the whole tile is skipped
     const U* sm = reinterpret_cast<const U*>(smem);
@@ -643,7 +668,7 @@ __global__ void __launch_bounds__(S::NT, col_tma_min_blocks<S>(KIND))
     fwt_col_tma_kernel(const __grid_constant__ TmaPassParams tp) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bar;
-  TmaMover<S> mv(tp, smem_raw, &bar);
+  TmaMover<S, (KIND == 1 || KIND == 3) ? 8 : 4> mv(tp, smem_raw, &bar);
   tile_body<S, KIND>(tp.p, smem_raw, mv, StaticBits<S>(tp.p));
 }
 

@@ -242,7 +242,7 @@ cudaError_t launch_col_tma(const PassParams& p, long long tiles, int ncomp, cuda
   if (rows > 0xffffffffull) return cudaErrorInvalidValue;
   const cuuint64_t dims[2] = {1ull << p.stride_log, rows};
   const cuuint64_t strides[1] = {(cuuint64_t)esz << p.stride_log};
-  const cuuint32_t box[2] = {1u << S::TS, (cuuint32_t)TmaMover<S>::BOXR};
+  const cuuint32_t box[2] = {1u << S::TS, (cuuint32_t)TmaMover<S, (KIND == 1 || KIND == 3) ? 8 : 4>::BOXR};
   const cuuint32_t estr[2] = {1, 1};
   TmaPassParams tp;
   tp.p = p;
