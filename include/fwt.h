@@ -149,6 +149,21 @@ int fwt_phase_c32(const float* re_in, const float* im_in, const float* theta,
                   int normalize, fwt_stream_t stream);
 
 /*
+ * The same for complex fp64 with fp64 angles: theta is a DEVICE array of doubles,
+ * 16-byte aligned, theta_stride even when n >= 1.  The phase comes from the
+ * double-precision sincos, applied element by element into the outputs, and the
+ * fp64 transform then runs in place on them (one extra read and write of the data:
+ * fusing the phase into the fixed-point row pass would make the CTAs of both parts
+ * evaluate every sine and cosine on the fp64 unit, which costs more).  The relative
+ * L2 error per vector stays below 1e-12 of the exact result for angles of moderate
+ * size (|theta| up to about 1e3; the phase error grows with |theta| as the sincos
+ * argument's own rounding does).  Other arguments and errors as fwt_phase_c32.
+ */
+int fwt_phase_c64(const double* re_in, const double* im_in, const double* theta,
+                  int64_t theta_stride, double* re_out, double* im_out, int n, int64_t batch,
+                  int normalize, fwt_stream_t stream);
+
+/*
  * Host-buffer transform: the same operation as fwt_batched_* on arrays in HOST
  * memory, copied to the device, transformed and copied back.  (The pages describe
  * the on-device transform only; this is the end-to-end form of it.)

@@ -62,8 +62,10 @@ def library() -> ctypes.CDLL:
             f = getattr(lib, name)
             f.argtypes = [vp, vp, vp, vp, ci, i64, ctypes.c_uint32, ci, vp]
             f.restype = ci
-        lib.fwt_phase_c32.argtypes = [vp, vp, vp, i64, vp, vp, ci, i64, ci, vp]
-        lib.fwt_phase_c32.restype = ci
+        for name in ("fwt_phase_c32", "fwt_phase_c64"):
+            f = getattr(lib, name)
+            f.argtypes = [vp, vp, vp, i64, vp, vp, ci, i64, ci, vp]
+            f.restype = ci
         for name in ("fwt_host_c32", "fwt_host_c64", "fwt_host_i32"):
             f = getattr(lib, name)
             f.argtypes = [vp, vp, vp, vp, ci, i64, ci, vp, ctypes.c_size_t, vp]
@@ -162,6 +164,12 @@ def fwt_mask_i32(re_in, im_in, re_out, im_out, n, batch, mask, normalize, stream
                                   stream)
 
 
+def fwt_phase_c64(re_in, im_in, theta, theta_stride, re_out, im_out, n, batch, normalize,
+                  stream) -> int:
+    return library().fwt_phase_c64(re_in, im_in, theta, theta_stride, re_out, im_out, n, batch,
+                                   int(normalize), stream)
+
+
 def fwt_phase_c32(re_in, im_in, theta, theta_stride, re_out, im_out, n, batch, normalize,
                   stream) -> int:
     return library().fwt_phase_c32(re_in, im_in, theta, theta_stride, re_out, im_out, n, batch,
@@ -210,16 +218,17 @@ def fwt_host_workspace_bytes(dtype, n, batch, with_im=True) -> int:
 
 
 def phase_transform(re, im, theta, out_re=None, out_im=None, normalize: bool = True, stream=None):
-    """y = s * H (e^{i theta} . x) for fp32 CUDA tensors of shape (batch, 2^n).
+    """y = s * H (e^{i theta} . x) for float32 or float64 CUDA tensors of shape
+    (batch, 2^n) (fwt_phase_c32 / fwt_phase_c64).
 
-    ``theta`` holds fp32 angles: shape (batch, 2^n) (one row per vector) or (2^n,) /
-    (1, 2^n) (shared by the batch).  Returns (out_re, out_im)."""
+    ``theta`` holds angles of the same dtype: shape (batch, 2^n) (one row per
+    vector) or (2^n,) / (1, 2^n) (shared by the batch).  Returns (out_re, out_im)."""
     import torch
 
-    if re.dtype != torch.float32 or im is None or im.dtype != torch.float32:
-        raise TypeError("phase_transform takes float32 re and im")
-    if theta.dtype != torch.float32 or not theta.is_cuda or not theta.is_contiguous():
-        raise ValueError("theta must be a contiguous float32 CUDA tensor")
+    if im is None or re.dtype not in (torch.float32, torch.float64) or im.dtype != re.dtype:
+        raise TypeError("phase_transform takes float32 or float64 re and im of one dtype")
+    if theta.dtype != re.dtype or not theta.is_cuda or not theta.is_contiguous():
+        raise ValueError("theta must be a contiguous CUDA tensor of the data's dtype")
     batch, N = re.shape
     n = int(N).bit_length() - 1
     if N < 1 or (1 << n) != N:
@@ -238,11 +247,13 @@ def phase_transform(re, im, theta, out_re=None, out_im=None, normalize: bool = T
     if stream is None:
         stream = torch.cuda.current_stream(re.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    entry, name = ((fwt_phase_c64, "fwt_phase_c64") if re.dtype == torch.float64
+                   else (fwt_phase_c32, "fwt_phase_c32"))
     with torch.cuda.device(re.device):
-        st = fwt_phase_c32(re.data_ptr(), im.data_ptr(), theta.data_ptr(), stride, out_re.data_ptr(),
-                           out_im.data_ptr(), n, batch, normalize, handle)
+        st = entry(re.data_ptr(), im.data_ptr(), theta.data_ptr(), stride, out_re.data_ptr(),
+                   out_im.data_ptr(), n, batch, normalize, handle)
     if st != FWT_OK:
-        raise FwtError(st, f"fwt_phase_c32(n={n}, batch={batch})")
+        raise FwtError(st, f"{name}(n={n}, batch={batch})")
     return out_re, out_im
 
 

@@ -610,6 +610,38 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
   return FWT_OK;
 }
 
+// y = s * H (e^{i theta} . x), fp64: the phase element by element into the outputs
+// (double sincos on the fp64 unit; fusing it into the fixed-point row pass would
+// make the CTAs of both parts evaluate every sine and cosine), then the fp64
+// transform in place.
+int run_phase_c64(const double* re_in, const double* im_in, const double* theta,
+                  int64_t theta_stride, double* re_out, double* im_out, int n, int64_t batch,
+                  int normalize, cudaStream_t stream) {
+  if (n < 0 || n > 30 || batch < 0 || theta_stride < 0) return FWT_ERR_INVALID_ARG;
+  if (batch == 0) return FWT_OK;
+  if (!im_in || !im_out || !theta) return FWT_ERR_INVALID_ARG;
+  bool has_im = false;
+  int st = check_arrays(FWT_C64, re_in, im_in, re_out, im_out, n, batch, has_im);
+  if (st != FWT_OK) return st;
+  if ((uintptr_t)theta & 15u) return FWT_ERR_MISALIGNED;
+  if (n >= 1 && theta_stride % 2 != 0) return FWT_ERR_MISALIGNED;  // 16-byte angle pairs
+  const long long th_elems = (theta_stride == 0 ? 0 : (long long)(batch - 1)) * theta_stride + (1ll << n);
+  const size_t th_bytes = (size_t)th_elems * 8;
+  const size_t bytes = (size_t)((long long)batch << n) * 8;
+  if (overlaps2(theta, th_bytes, re_out, bytes) || overlaps2(theta, th_bytes, im_out, bytes))
+    return FWT_ERR_INVALID_ARG;
+  cudaError_t err = ensure_device();
+  const int sms = prefetch_ahead() / 3;  // SMs of the current device
+  if (err == cudaSuccess)
+    err = launch_phase_apply_c64(re_in, im_in, theta, theta_stride, re_out, im_out, n, batch, sms,
+                                 stream);
+  if (err != cudaSuccess) {
+    g_last_cuda_error = (int)err;
+    return FWT_ERR_CUDA;
+  }
+  return run(FWT_C64, re_out, im_out, re_out, im_out, n, batch, 0, n, normalize, stream);
+}
+
 // y = s * H (e^{i theta} . x), fp32: a fused phase + row pass over the low
 // min(n, 13) bits, then in-place column passes over the rest.
 int run_phase(const float* re_in, const float* im_in, const float* theta, int64_t theta_stride,
@@ -793,6 +825,13 @@ int fwt_mask_c64(const double* re_in, const double* im_in, double* re_out, doubl
 int fwt_mask_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, int32_t* im_out,
                  int n, int64_t batch, uint32_t mask, int normalize, fwt_stream_t stream) {
   return fwt::run_mask(FWT_I32, re_in, im_in, re_out, im_out, n, batch, mask, normalize, stream);
+}
+
+int fwt_phase_c64(const double* re_in, const double* im_in, const double* theta,
+                  int64_t theta_stride, double* re_out, double* im_out, int n, int64_t batch,
+                  int normalize, fwt_stream_t stream) {
+  return fwt::run_phase_c64(re_in, im_in, theta, theta_stride, re_out, im_out, n, batch,
+                            normalize, (cudaStream_t)stream);
 }
 
 int fwt_phase_c32(const float* re_in, const float* im_in, const float* theta,

@@ -499,6 +499,10 @@ KernelEntry small_entry() {
   return e;
 }
 
+// fp64 diagonal phase, element by element (rows_c64.cu); sms sizes the grid.
+cudaError_t launch_phase_apply_c64(const double* re_in, const double* im_in, const double* theta,
+                                   long long theta_stride, double* re_out, double* im_out, int n,
+                                   long long batch, int sms, cudaStream_t st);
 cudaError_t read_device_error_c32(unsigned int* out);
 // Records a failed CUDA call for fwt_last_cuda_error() (calling thread).
 void set_last_cuda_error(int err);
