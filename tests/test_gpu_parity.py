@@ -434,3 +434,40 @@ def test_concurrent_host_threads():
     for t in threads:
         t.join()
     assert not errors, errors
+
+
+def test_random_plans_widths_and_movers():
+    """Seeded random cases over n = 14..23: a random valid 2- or 3-factor split, column
+    width, TMA mode, batch, in or out of place, normalised or not."""
+    rng = np.random.default_rng(2024)
+    done = 0
+    try:
+        while done < 30:
+            dtype = ["c32", "c64", "i32"][rng.integers(3)]
+            n = int(rng.integers(14, 24))
+            cb = int(rng.choice([16, 32, 64, 128]))
+            tma = int(rng.integers(0, 3))
+            if cb == 16:
+                tma = 2
+            fwt.set_tma(tma)
+            fwt.set_column_bytes(dtype, cb)
+            plans = _valid_plans(n, dtype)
+            if not plans:
+                continue
+            plan = plans[int(rng.integers(len(plans)))]
+            fwt.set_plan(n, dtype, plan)
+            batch = int(rng.integers(1, 4))
+            norm = dtype != "i32" and bool(rng.integers(2))
+            re, im = inputs.random_pair(n, batch, dtype, seed=int(rng.integers(1 << 30)))
+            ore, oim = oracle.fwt_complex(re, im, normalize=norm, nthreads=host_threads())
+            gre, gim = gpu_transform(re, im, norm, inplace=bool(rng.integers(2)))
+            assert_matches(dtype, gre, gim, ore, oim, f"{dtype} n={n} plan={plan} cb={cb} tma={tma}")
+            fwt.set_plan(n, dtype, None)
+            done += 1
+    finally:
+        for dt in ("c32", "c64", "i32"):
+            fwt.set_column_bytes(dt, 0)
+            for n in range(14, 24):
+                fwt.set_plan(n, dt, None)
+        fwt.set_tma(fwt.TMA_AUTO)
+    assert fwt.device_status() == fwt.FWT_OK
