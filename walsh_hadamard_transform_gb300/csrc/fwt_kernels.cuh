@@ -9,7 +9,7 @@
 //                 vectors).  This is the whole transform when n fits a tile, and
 //                 the I (x) H_b factor of the Kronecker split otherwise.
 //   column tiles: bits [L, L + K) of each vector; a tile is 2^K rows spaced 2^L
-//                 elements apart, times one 128-byte segment of contiguous
+//                 elements apart, times one 16- to 128-byte segment of contiguous
 //                 columns.  This is the H_a (x) I factor of the Kronecker split
 //                 ("[QDP] [feature] Pr4 kronecker fwt", section "Why submit PR4",
 //                 deliverables: Y = (H_{n1} (x) I)(I (x) H_{n2}) X; iThome "Day
@@ -21,10 +21,16 @@
 // fp64 runs its butterflies exactly in 64-bit fixed point on the integer units
 // (GB300's fp64 add rate is about 1/64 of its fp32 rate, while 64-bit integer
 // adds run near the fp32 rate): the tile's largest binary exponent sets a common
-// scale, every element is converted to an int64 with 61 - K fraction bits of
-// headroom below it, the K stages run exactly, and each result is rounded once
-// back to fp64 (round to nearest even).  Both conversions use integer bit
-// arithmetic only.  A tile holding an Inf or NaN takes a plain fp64 path instead.
+// scale, every element is converted to an int64 with 61 - K fraction bits (integer
+// bit arithmetic), the K stages run exactly, and each result is rounded once back
+// to fp64 (the hardware int64 -> fp64 conversion, round to nearest even, then an
+// exponent-field add; an all-integer exact rounding where results could be
+// subnormal or overflow).  A tile holding an Inf or NaN takes a plain fp64 path.
+//
+// Tiles are staged three ways: 16-byte vector loads and stores (DirectMover),
+// untiled bulk copies of whole contiguous tiles (BulkMover, fp64 row tiles), and
+// TMA 2-D tensor copies of strided column tiles (TmaMover); the staged kernels run
+// three CTAs an SM at 80 registers a thread.
 #pragma once
 
 #include <cstdint>

@@ -27,7 +27,7 @@ struct KernelEntry {
   int K;      // transformed index bits of the pass
   int TB;     // log2 elements per tile (0 for the small kernel)
   int TS;     // first transformed tile bit (column tiles: log2 columns per tile)
-  int col_bytes;  // column tiles: bytes of contiguous columns per row (32, 64 or 128)
+  int col_bytes;  // column tiles: bytes of contiguous columns per row (16 .. 128)
   int tma;        // column tiles staged through shared memory by TMA copies
   int threads;
   size_t smem;  // dynamic shared memory per CTA
