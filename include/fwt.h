@@ -214,7 +214,9 @@ size_t fwt_host_workspace_bytes(int dtype, int n, int64_t batch, int with_im);
  * static device memory, a file-scope __device__ array of
  * fwt_host_static_workspace_bytes() bytes per device that is part of the module
  * image (set up with cudaGetSymbolAddress on first use on a device), so nothing is
- * allocated at run time.  The pages have no counterpart of this entry point: it is
+ * allocated at run time.  The array occupies that much device memory once its
+ * module is loaded: at the first call under CUDA's lazy module loading (the
+ * default), at context creation under eager loading.  The pages have no counterpart of this entry point: it is
  * a convenience of the host-buffer path.  Same operation, arguments, layout,
  * in-place rules, asynchrony and errors as fwt_host_*; a vector (both parts) larger
  * than the static buffer is FWT_ERR_INVALID_ARG.  Calls share the buffer: each call
