@@ -329,7 +329,9 @@ def run_ours(args):
         algo = 2 * parts[pi].bytes_in  # every pass reads and writes the whole batch once
         if args.phase and li == [i for i, o in enumerate(owners) if o == pi][0]:
             algo += algo // 4  # the first pass also reads the angles (fp32, one per amplitude)
-        kernels.append({"kernel": nm, "mean_ms": mean_ms, "total_ms": sum(per_kernel[li]),
+        kernels.append({"kernel": nm, "mean_ms": mean_ms,
+                        "median_ms": statistics.median(per_kernel[li]), "min_ms": min(per_kernel[li]),
+                        "total_ms": sum(per_kernel[li]),
                         "algo_bytes_per_launch": algo, "gbs": algo / (mean_ms * 1e-3) / 1e9})
     top = max(kernels, key=lambda k: k["total_ms"])
     traffic = ncu_traffic(top["kernel"])
