@@ -334,7 +334,21 @@ def run_ours(args):
                         "total_ms": sum(per_kernel[li]),
                         "algo_bytes_per_launch": algo, "gbs": algo / (mean_ms * 1e-3) / 1e9})
     top = max(kernels, key=lambda k: k["total_ms"])
-    traffic = ncu_traffic(top["kernel"])
+    # the committed ncu traffic is per launch of the default batch
+    traffic_of = (lambda key: ncu_traffic(key)) if args.batch <= 0 else (lambda key: None)
+    traffic = traffic_of(top["kernel"])
+    # DRAM bytes per vector: the pass model (each pass reads and writes the vector
+    # once), the one-round-trip ideal, and the ncu-measured bytes when every pass of
+    # the part has a current capture
+    per_vector = []
+    for pi, w in enumerate(parts):
+        ks = [k for k, o in zip(kernels, owners) if o == pi]
+        vec = w.bytes_in // w.batch  # re + im of one vector
+        meas = [traffic_of(k["kernel"]) for k in ks]
+        per_vector.append({"part": w.name, "passes": len(ks), "model": 2 * len(ks) * vec,
+                           "one_round_trip": 2 * vec,
+                           "measured": (sum(meas) // w.batch
+                                        if meas and all(m is not None for m in meas) else None)})
     roofline = {"bound": "hbm", "achieved": round(top["gbs"], 1), "peak": peak, "unit": "GB/s",
                 "frac": round(top["gbs"] / peak, 4), "traffic": traffic,
                 "kernel": top["kernel"], "peak_source": peak_src,
@@ -363,6 +377,7 @@ def run_ours(args):
         "hbm_gbs_effective_per_gpu": round(algo_bytes_step * args.steps / (elapsed_ms / 1e3) / 1e9, 1),
         "kernels": [{k: (round(v, 4) if isinstance(v, float) else v) for k, v in kk.items()} for kk in kernels],
         "roofline": roofline,
+        "dram_bytes_per_vector": per_vector,
         "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
     }
