@@ -100,7 +100,8 @@ def test_plans(lib):
         assert fwt.plan_factors(28, "i32") == [13, 8, 7]
         assert fwt.plan_factors(25, "c64") == [14, 11]
         assert fwt.plan_factors(26, "c64") == [12, 6, 8]
-        assert fwt.plan_factors(30, "c64") == [13, 10, 7]
+        assert fwt.plan_factors(27, "c64") == [12, 8, 7]
+        assert fwt.plan_factors(30, "c64") == [12, 9, 9]
     assert lib.fwt_plan_passes(31, 0) == -1 and lib.fwt_plan_passes(10, 7) == -1
 
 

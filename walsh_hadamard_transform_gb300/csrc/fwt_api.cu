@@ -64,15 +64,20 @@ struct Plan {
   int nf = 0;
   int bits[3] = {0, 0, 0};
   int col_bytes = 128;  // width of the column passes' row segments
-  int tma = 1;          // TMA-staged column passes: 0 never, 1 for K >= 10, 2 always
+  int tma = 1;          // TMA-staged column passes: 0 never, 1 auto, 2 always
+  int tma_mask = -1;    // auto, measured plans: factor f staged by TMA iff bit f is set
   const KernelEntry* cluster = nullptr;  // one-pass cluster kernel instead of the factors
 };
 
 // TMA staging pays for column tiles with many rows (long strided walks); short
-// tiles are faster with plain vector loads (measured on GB300).
+// tiles are faster with plain vector loads (measured on GB300), unless a measured
+// plan says otherwise for its factor f (f < 0: a pass outside the plan's factors).
 // 16-byte segments exist only as TMA tiles.
-int col_tma(const Plan& p, int K) {
-  return p.tma == 2 || p.col_bytes == 16 || (p.tma == 1 && K >= 10) ? 1 : 0;
+int col_tma(const Plan& p, int f, int K) {
+  if (p.tma == 2 || p.col_bytes == 16) return 1;
+  if (p.tma == 0) return 0;
+  if (p.tma_mask >= 0 && f >= 0) return (p.tma_mask >> f) & 1;
+  return K >= 10 ? 1 : 0;
 }
 
 std::mutex g_plan_mu;
@@ -103,7 +108,7 @@ bool plan_valid(int n, int dtype, const Plan& p) {
         return false;
       }
     } else {
-      const KernelEntry* e = find_kernel(dtype, KIND_COL, k, p.col_bytes, col_tma(p, k));
+      const KernelEntry* e = find_kernel(dtype, KIND_COL, k, p.col_bytes, col_tma(p, f, k));
       if (!e) return false;
       if (sum < e->TS) return false;  // a column segment must fit in one row
     }
@@ -114,8 +119,9 @@ bool plan_valid(int n, int dtype, const Plan& p) {
 
 // Splits measured faster than the general rule (GB300, a sweep of every two-factor
 // split, column width and TMA mode at 2^26 elements a part for n <= 23, of every
-// split and width at 2^28 for larger n).
-//  * fp64 n = 15..23: a row factor of 9..12 bits and a column factor of 6..11 at 64-
+// split and width at 2^28 for larger n, and of every fp64 three-factor split with
+// TMA staging chosen per factor for n = 26..30).
+//  * fp64 n = 15..22: a row factor of 9..12 bits and a column factor of 6..11 at 64-
 //    or 128-byte segments, every column tile staged by TMA (the TMA column kernel
 //    runs three CTAs an SM; the direct one two): passes of few bits are HBM-bound
 //    (~6.7 TB/s), 15-25% faster than the general rule.
@@ -125,27 +131,30 @@ bool plan_valid(int n, int dtype, const Plan& p) {
 //    need narrow segments.
 //  * fp64 from n = 25: tiles of 2^14 elements run one 512-thread CTA (or a CTA pair)
 //    at about half the rate of the 2^13-element tiles, so from n = 26 three passes
-//    over tiles of at most 2^13 elements win.
+//    over tiles of at most 2^13 elements win: a 12-bit row factor and two column
+//    factors at 128 bytes, the middle one TMA-staged (~6.4 TB/s), the top one staged
+//    where that measured faster (8-11% below the earlier per-plan TMA rule).
 struct MeasuredSplit {
   bool fp64;
   int n, nf, bits[3], col_bytes;
-  bool tma_always;  // every column factor TMA-staged (when the TMA mode is auto)
+  int tma_factors;  // column factors staged by TMA (bit f), when the TMA mode is
+                    // auto; 0: the K >= 10 rule
 };
 constexpr MeasuredSplit kMeasuredSplits[] = {
-    {true, 15, 2, {9, 6, 0}, 128, true},    {true, 16, 2, {10, 6, 0}, 128, true},
-    {true, 17, 2, {10, 7, 0}, 128, true},   {true, 18, 2, {10, 8, 0}, 128, true},
-    {true, 19, 2, {12, 7, 0}, 128, true},   {true, 20, 2, {12, 8, 0}, 128, true},
-    {true, 21, 2, {11, 10, 0}, 64, true},   {true, 22, 2, {12, 10, 0}, 64, true},
-    {true, 23, 2, {12, 11, 0}, 32, false},
-    {false, 18, 2, {12, 6, 0}, 128, false}, {false, 19, 2, {13, 6, 0}, 128, false},
-    {false, 20, 2, {13, 7, 0}, 128, false}, {false, 21, 2, {13, 8, 0}, 128, false},
-    {false, 22, 2, {14, 8, 0}, 128, false},
-    {false, 25, 2, {14, 11, 0}, 32, false}, {false, 26, 2, {15, 11, 0}, 32, false},
-    {false, 27, 3, {12, 7, 8}, 128, false}, {false, 28, 3, {13, 8, 7}, 128, false},
-    {false, 29, 3, {13, 8, 8}, 128, false}, {false, 30, 3, {14, 8, 8}, 128, false},
-    {true, 25, 2, {14, 11, 0}, 32, false},  {true, 26, 3, {12, 6, 8}, 128, false},
-    {true, 27, 3, {12, 7, 8}, 128, false},  {true, 28, 3, {12, 8, 8}, 128, false},
-    {true, 29, 3, {12, 10, 7}, 64, false},  {true, 30, 3, {13, 10, 7}, 64, false},
+    {true, 15, 2, {9, 6, 0}, 128, 0b10},    {true, 16, 2, {10, 6, 0}, 128, 0b10},
+    {true, 17, 2, {10, 7, 0}, 128, 0b10},   {true, 18, 2, {10, 8, 0}, 128, 0b10},
+    {true, 19, 2, {12, 7, 0}, 128, 0b10},   {true, 20, 2, {12, 8, 0}, 128, 0b10},
+    {true, 21, 2, {11, 10, 0}, 64, 0b10},   {true, 22, 2, {12, 10, 0}, 64, 0b10},
+    {true, 23, 2, {12, 11, 0}, 32, 0},
+    {false, 18, 2, {12, 6, 0}, 128, 0}, {false, 19, 2, {13, 6, 0}, 128, 0},
+    {false, 20, 2, {13, 7, 0}, 128, 0}, {false, 21, 2, {13, 8, 0}, 128, 0},
+    {false, 22, 2, {14, 8, 0}, 128, 0},
+    {false, 25, 2, {14, 11, 0}, 32, 0}, {false, 26, 2, {15, 11, 0}, 32, 0},
+    {false, 27, 3, {12, 7, 8}, 128, 0}, {false, 28, 3, {13, 8, 7}, 128, 0},
+    {false, 29, 3, {13, 8, 8}, 128, 0}, {false, 30, 3, {14, 8, 8}, 128, 0},
+    {true, 25, 2, {14, 11, 0}, 32, 0},      {true, 26, 3, {12, 6, 8}, 128, 0b110},
+    {true, 27, 3, {12, 8, 7}, 128, 0b010},  {true, 28, 3, {12, 8, 8}, 128, 0b010},
+    {true, 29, 3, {12, 8, 9}, 128, 0b110},  {true, 30, 3, {12, 9, 9}, 128, 0b110},
 };
 
 Plan default_plan(int n, int dtype) {
@@ -164,7 +173,7 @@ Plan default_plan(int n, int dtype) {
       q.nf = ms.nf;
       for (int f = 0; f < 3; ++f) q.bits[f] = ms.bits[f];
       q.col_bytes = ms.col_bytes;
-      if (ms.tma_always && q.tma == 1) q.tma = 2;
+      if (ms.tma_factors && q.tma == 1) q.tma_mask = ms.tma_factors;
       if (plan_valid(n, dtype, q)) return q;
     }
   }
@@ -334,7 +343,7 @@ struct PassSpec {
 const KernelEntry* column_kernel(int dtype, int K, int L, const Plan& plan) {
   const int widths[5] = {plan.col_bytes, 128, 64, 32, 16};
   for (int cb : widths) {
-    for (int tma : {col_tma(plan, K), 1 - col_tma(plan, K)}) {
+    for (int tma : {col_tma(plan, -1, K), 1 - col_tma(plan, -1, K)}) {
       const KernelEntry* e = find_kernel(dtype, KIND_COL, K, cb, tma);
       if (e && L >= e->TS) return e;
     }
@@ -388,7 +397,7 @@ bool full_passes(int n, int dtype, const Plan& plan, std::vector<PassSpec>& out)
     const int K = plan.bits[f];
     PassSpec ps{nullptr, L, 0, 0};
     if (f == 0) ps.e = row_kernel(dtype, K);
-    else ps.e = find_kernel(dtype, KIND_COL, K, plan.col_bytes, col_tma(plan, K));
+    else ps.e = find_kernel(dtype, KIND_COL, K, plan.col_bytes, col_tma(plan, f, K));
     if (!ps.e) return false;
     out.push_back(ps);
     L += K;
