@@ -138,7 +138,9 @@ int fwt_mask_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, in
  * angles are an input: a DEVICE array of fp32 radians, theta_stride elements
  * between vectors (0: one row of 2^n angles shared by the batch; 2^n: one row per
  * vector).  theta must be 16-byte aligned, theta_stride a multiple of 4 when
- * n >= 2, and the angle array must not overlap the outputs.  Phases come from
+ * n >= 2, and the angle array must not overlap the outputs (a theta_stride whose
+ * angle extent, (batch - 1) * theta_stride + 2^n elements, does not fit in 64-bit
+ * byte offsets is FWT_ERR_INVALID_ARG).  Phases come from
  * sincosf; the rotation is fused into the first pass (one read of x and theta,
  * one write), later passes as in fwt_batched_c32.  The relative L2 error per
  * vector stays within 2e-6 of the exact result.  Other arguments, in-place rules
@@ -255,6 +257,14 @@ int fwt_plan_passes(int n, int dtype);
  * -1 for invalid input.  The factors sum to n.
  */
 int fwt_plan_factors(int n, int dtype, int* bits, int max_factors);
+
+/*
+ * Plan log: with the environment variable FWT_LOG set to anything but "" or "0"
+ * (read once per process), every transform, bit-range, bit-mask and phase call
+ * prints one line to stderr before it launches: the dtype, n, batch and each planned
+ * pass (kind, transformed bits K, tile size, and for column passes the row stride,
+ * segment width and mover).  Host-buffer calls print one line per chunk.
+ */
 
 /*
  * Tuning / testing: replace the plan for (n, dtype) by the given Kronecker

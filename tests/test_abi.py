@@ -247,3 +247,19 @@ def test_mask_argument_errors_before_launch(lib, fn):
     assert f(None, None, None, None, 4, 0, 0b101, norm, None) == fwt.FWT_OK  # empty batch
     assert f(a + 4, b, c, d, 4, 1, 0b101, norm, None) == fwt.FWT_ERR_MISALIGNED
     assert f(a, b, a + 16, d, 4, 1, 0b101, norm, None) == fwt.FWT_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("fn", ["fwt_phase_c32", "fwt_phase_c64"])
+def test_phase_argument_errors_before_launch(lib, fn):
+    f = getattr(fwt, fn)
+    a, b, c, d, th = A, A + GiB, A + 2 * GiB, A + 3 * GiB, A + 4 * GiB
+    E = fwt.FWT_ERR_INVALID_ARG
+    assert f(a, b, th, -4, c, d, 4, 2, 1, None) == E             # negative stride
+    assert f(a, b, th, 16, c, d, 31, 1, 1, None) == E            # n > 30
+    assert f(a, b, None, 16, c, d, 4, 2, 1, None) == E           # no angles
+    assert f(a, None, th, 16, c, None, 4, 2, 1, None) == E       # both parts required
+    assert f(a, b, th + 4, 16, c, d, 4, 2, 1, None) == fwt.FWT_ERR_MISALIGNED
+    assert f(a, b, th, 1, c, d, 4, 2, 1, None) == fwt.FWT_ERR_MISALIGNED  # odd stride
+    assert f(a, b, th, 1 << 61, c, d, 4, 3, 1, None) == E        # angle extent overflows
+    assert f(a, b, c, 16, c, d, 4, 2, 1, None) == E              # angles overlap re_out
+    assert f(None, None, None, 0, None, None, 4, 0, 1, None) == fwt.FWT_OK  # empty batch

@@ -471,3 +471,33 @@ def test_random_plans_widths_and_movers():
                 fwt.set_plan(n, dt, None)
         fwt.set_tma(fwt.TMA_AUTO)
     assert fwt.device_status() == fwt.FWT_OK
+
+
+def test_plan_log_environment_variable():
+    """FWT_LOG=1 prints one plan line a call to stderr (a fresh process: the variable
+    is read once); without it nothing is printed."""
+    import os
+    import subprocess
+    import sys
+
+    code = ("import torch, walsh_hadamard_transform_gb300 as fwt\n"
+            "a = torch.randn(2, 1 << 24, dtype=torch.float64, device='cuda')\n"
+            "fwt.transform(a, a.clone())\n"
+            "x = torch.randn(3, 1 << 12, device='cuda')\n"
+            "fwt.transform(x, x.clone(), bits=(3, 5))\n"
+            "torch.cuda.synchronize()\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for value, expect in (("1", True), ("0", False)):
+        env = dict(os.environ, FWT_LOG=value)
+        r = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                           text=True, timeout=300)
+        assert r.returncode == 0, r.stderr[-2000:]
+        lines = [ln for ln in r.stderr.splitlines() if ln.startswith("fwt: ")]
+        if not expect:
+            assert lines == []
+            continue
+        assert len(lines) == 2, r.stderr[-2000:]
+        assert lines[0].startswith("fwt: transform c64 n=24 batch=2 passes=2 | row K=13")
+        assert "| col K=11 tile=2^13 stride=2^13 32B tma" in lines[0]
+        assert lines[1].startswith("fwt: bits c32 n=12 batch=3 passes=1 | rowbits")
+        assert "bits=[3,8)" in lines[1]

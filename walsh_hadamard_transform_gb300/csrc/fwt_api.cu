@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -470,6 +471,43 @@ bool mask_passes(int n, int dtype, uint32_t mask, const Plan& plan, std::vector<
   return true;
 }
 
+// FWT_LOG set (and not "0") in the environment: every transform call prints its
+// passes to stderr, one line a call (read once per process).
+bool log_plans() {
+  static const bool on = [] {
+    const char* v = std::getenv("FWT_LOG");
+    return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
+  }();
+  return on;
+}
+
+void log_plan(const char* what, int dtype, int n, int64_t batch, const std::vector<PassSpec>& passes) {
+  static const char* const kDtype[3] = {"c32", "c64", "i32"};
+  static const char* const kKind[6] = {"small", "row", "col", "rowbits", "phase", "cluster"};
+  char line[512];
+  int len = snprintf(line, sizeof line, "fwt: %s %s n=%d batch=%lld passes=%d", what,
+                     kDtype[dtype], n, (long long)batch, (int)passes.size());
+  for (const PassSpec& ps : passes) {
+    const KernelEntry* e = ps.e;
+    if (len < 0 || len >= (int)sizeof line) break;
+    len += snprintf(line + len, sizeof line - len, " | %s K=%d tile=2^%d", kKind[e->kind], e->K,
+                    e->TB);
+    if (len < (int)sizeof line && e->kind == KIND_COL)
+      len += snprintf(line + len, sizeof line - len, " stride=2^%d %dB %s", ps.L, e->col_bytes,
+                      e->tma ? "tma" : "direct");
+    if (len < (int)sizeof line && e->kind == KIND_CLUSTER)
+      len += snprintf(line + len, sizeof line - len, " ctas=%d", 1 << e->TS);
+    if (len < (int)sizeof line && e->kind == KIND_ROWBITS) {
+      if (ps.mask)
+        len += snprintf(line + len, sizeof line - len, " mask=0x%x", ps.mask);
+      else
+        len += snprintf(line + len, sizeof line - len, " bits=[%d,%d)", ps.bits_lo,
+                        ps.bits_lo + ps.bits_k);
+    }
+  }
+  fprintf(stderr, "%s\n", line);
+}
+
 int check_arrays(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out,
                  int n, int64_t batch, bool& has_im) {
   const int esz = elem_size(dtype);
@@ -522,6 +560,9 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
   } else if (!range_passes(n, dtype, lo, k, plan, passes)) {
     return FWT_ERR_UNSUPPORTED;
   }
+
+  if (log_plans())
+    log_plan(mask ? "mask" : (whole ? "transform" : "bits"), dtype, n, batch, passes);
 
   PassParams p{};
   const int ahead = prefetch_ahead();
@@ -634,6 +675,8 @@ int run_phase_c64(const double* re_in, const double* im_in, const double* theta,
   if (st != FWT_OK) return st;
   if ((uintptr_t)theta & 15u) return FWT_ERR_MISALIGNED;
   if (n >= 1 && theta_stride % 2 != 0) return FWT_ERR_MISALIGNED;  // 16-byte angle pairs
+  if (batch > 1 && theta_stride > (INT64_MAX / 8 - (1ll << n)) / (batch - 1))
+    return FWT_ERR_INVALID_ARG;  // the angles' extent would overflow
   const long long th_elems = (theta_stride == 0 ? 0 : (long long)(batch - 1)) * theta_stride + (1ll << n);
   const size_t th_bytes = (size_t)th_elems * 8;
   const size_t bytes = (size_t)((long long)batch << n) * 8;
@@ -664,6 +707,8 @@ int run_phase(const float* re_in, const float* im_in, const float* theta, int64_
   if (st != FWT_OK) return st;
   if ((uintptr_t)theta & 15u) return FWT_ERR_MISALIGNED;
   if (n >= 2 && theta_stride % 4 != 0) return FWT_ERR_MISALIGNED;  // 16-byte angle vectors
+  if (batch > 1 && theta_stride > (INT64_MAX / 4 - (1ll << n)) / (batch - 1))
+    return FWT_ERR_INVALID_ARG;  // the angles' extent would overflow
   const long long th_elems = (theta_stride == 0 ? 0 : (long long)(batch - 1)) * theta_stride + (1ll << n);
   const size_t th_bytes = (size_t)th_elems * 4;
   const size_t bytes = (size_t)((long long)batch << n) * 4;
@@ -690,6 +735,7 @@ int run_phase(const float* re_in, const float* im_in, const float* theta, int64_
   if (!e0) return FWT_ERR_UNSUPPORTED;
   passes.push_back(PassSpec{e0, 0, 0, 0});
   if (n > k1 && !column_passes(FWT_C32, k1, n, plan, passes)) return FWT_ERR_UNSUPPORTED;
+  if (log_plans()) log_plan("phase", FWT_C32, n, batch, passes);
 
   PassParams p{};
   const double s = n % 2 == 0 ? std::ldexp(1.0, -n / 2) : std::ldexp(1.0, -(n - 1) / 2) / std::sqrt(2.0);
