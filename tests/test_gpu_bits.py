@@ -122,3 +122,23 @@ def test_bit_mask_argument_errors():
         fwt.transform(a, a.clone(), mask=1 << 5)
     with pytest.raises(ValueError):
         fwt.transform(a, a.clone(), mask=1, bits=(0, 1))
+
+
+@pytest.mark.parametrize("dtype", ["c32", "c64", "i32"])
+def test_out_of_place_ranges_on_16_byte_column_tiles(dtype):
+    """Ranges from bit 2 (4-byte types) or bit 1 (fp64) long enough for column passes:
+    at that row stride the only column tile is a 16-byte TMA tile, which runs in
+    place, so an out-of-place call copies the input to the output first.  Both forms
+    against the oracle."""
+    lo = 1 if dtype == "c64" else 2
+    n = 17
+    re, im = inputs.random_pair(n, 3, dtype, seed=77)
+    for k in (8, 9, 10, 12, n - lo):
+        for norm in ((False,) if dtype == "i32" else (True,)):
+            ore = oracle.fwt_bits(re, lo, k, normalize=norm)
+            oim = oracle.fwt_bits(im, lo, k, normalize=norm)
+            for inplace in (False, True):
+                gre, gim = _gpu_bits(re, im, lo, k, norm, inplace=inplace)
+                assert_matches(dtype, gre, gim, ore, oim,
+                               f"bits [{lo}, {lo + k}) n={n} in_place={inplace}")
+    assert fwt.device_status() == fwt.FWT_OK

@@ -357,6 +357,20 @@ const KernelEntry* column_kernel(int dtype, int K, int L, const Plan& plan) {
   return nullptr;
 }
 
+// A vector-load column kernel for K bits at row stride 2^L, preferring segments of
+// `prefer` bytes, or nullptr (16-byte segments exist only as TMA tiles).
+const KernelEntry* direct_column_kernel(int dtype, int K, int L, int prefer) {
+  for (int cb : {prefer, 128, 64, 32}) {
+    const KernelEntry* e = find_kernel(dtype, KIND_COL, K, cb, 0);
+    if (e && L >= e->TS) return e;
+  }
+  if (K <= 5) {  // short factors: wide segments of 2^(10-K) elements
+    const KernelEntry* e = find_kernel(dtype, KIND_COL, K, (1 << (10 - K)) * elem_size(dtype), 0);
+    if (e && L >= e->TS) return e;
+  }
+  return nullptr;
+}
+
 // Column passes over bits [L, hi), in as few factors as the plan's segment width
 // allows (near-equal sizes).
 bool column_passes(int dtype, int L, int hi, const Plan& plan, std::vector<PassSpec>& out) {
@@ -561,6 +575,23 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
     return FWT_ERR_UNSUPPORTED;
   }
 
+  // TMA-staged column tiles run in place.  An out-of-place call whose first pass is
+  // one loads that pass with 16-byte vectors where a tile shape exists for it; else
+  // (16-byte segments below the row stride: TMA tiles only) a row pass over no bits
+  // first copies the input into the output, and the column pass runs there in place.
+  const bool call_in_place = re_in == re_out && (!has_im || im_in == im_out);
+  if (!call_in_place && !passes.empty() && passes[0].e->kind == KIND_COL && passes[0].e->tma) {
+    const KernelEntry* d =
+        direct_column_kernel(dtype, passes[0].e->K, passes[0].L, passes[0].e->col_bytes);
+    if (d) {
+      passes[0].e = d;
+    } else {
+      const KernelEntry* copy = find_kernel(dtype, KIND_ROWBITS, 12);
+      if (!copy) return FWT_ERR_UNSUPPORTED;
+      passes.insert(passes.begin(), PassSpec{copy, 0, 0, 0});
+    }
+  }
+
   if (log_plans())
     log_plan(mask ? "mask" : (whole ? "transform" : "bits"), dtype, n, batch, passes);
 
@@ -620,13 +651,7 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
           p.out[c] = outs[part] ? (char*)outs[part] + off : nullptr;
           in_place &= p.in[c] == p.out[c];
         }
-        if (e->tma && !in_place) {  // TMA column tiles run in place; copy-in passes load directly
-          const KernelEntry* d = find_kernel(dtype, KIND_COL, e->K, e->col_bytes, 0);
-          if (!d) d = column_kernel(dtype, e->K, ps.L, Plan{0, {0, 0, 0}, 128, 0});
-          if (!d) return FWT_ERR_UNSUPPORTED;
-          e = d;
-          tiles = elems >> e->TB;
-        }
+        if (e->tma && !in_place) return FWT_ERR_UNSUPPORTED;  // planned away above
         p.stride_log = ps.L;
         p.bits_lo = ps.bits_lo;
         p.bits_k = ps.bits_k;
