@@ -293,7 +293,10 @@ int fwt_get_column_bytes(int dtype);
  * How column passes move their strided tiles: mode 2 stages every tile through
  * shared memory with TMA (cp.async.bulk.tensor) copies, 0 uses 16-byte vector
  * loads and stores, 1 (default) uses TMA for column factors of 10 or more bits
- * (tiles of 1024+ rows) and vector loads below.  Modes 1 and 2 also stage whole
+ * (tiles of 1024+ rows) and vector loads below, except in the measured default plans
+ * that choose the mover per column factor (fp64 n = 15..22 and 26..30).  16-byte
+ * column segments exist only as TMA tiles in every mode; an out-of-place call whose
+ * first pass needs one copies its input to the output first.  Modes 1 and 2 also stage whole
  * fp64 row tiles with untiled bulk copies (cp.async.bulk); mode 0 loads them with
  * vector loads.  All modes give identical results.  Affects default plans and
  * plans set afterwards.  Returns FWT_OK or
