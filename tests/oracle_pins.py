@@ -284,6 +284,27 @@ def pin_bit_mask(orc):
     assert np.array_equal(orc.fwt_mask(x, 0, normalize=True), x)
 
 
+def pin_complex_parts(orc):
+    """A split complex vector transforms part by part (H is real): the real output is
+    the dense popc product of the real input, the imaginary output that of the
+    imaginary input, for float and wrapping int32; an int32 vector without an
+    imaginary part gives none."""
+    rng = np.random.default_rng(57)
+    for n in (0, 1, 5, 9):
+        re, im = rng.standard_normal((2, 3, 1 << n))
+        gr, gi = orc.fwt_complex(re, im, normalize=True)
+        assert _rel(gr, dense.dense_fwt(re, normalize=True)) < 1e-14, f"real part n={n}"
+        assert _rel(gi, dense.dense_fwt(im, normalize=True)) < 1e-14, f"imaginary part n={n}"
+        ri, ii = rng.integers(-(2 ** 31), 2 ** 31, size=(2, 2, 1 << n), dtype=np.int64).astype(np.int32)
+        gr, gi = orc.fwt_complex(ri, ii, normalize=False)
+        for got, x in ((gr, ri), (gi, ii)):
+            ref = (dense.dense_fwt(x.astype(np.int64)) % (1 << 32)).astype(np.uint32).view(np.int32)
+            assert np.array_equal(got, ref), f"int32 part n={n}"
+        gr, gi = orc.fwt_complex(ri, None, normalize=False)
+        assert gi is None and np.array_equal(
+            gr, (dense.dense_fwt(ri.astype(np.int64)) % (1 << 32)).astype(np.uint32).view(np.int32))
+
+
 ORACLE_PINS = [
     pin_butterfly_vs_dense_float,
     pin_butterfly_vs_dense_int,
@@ -299,4 +320,5 @@ ORACLE_PINS = [
     pin_bit_range,
     pin_bit_mask,
     pin_phase_then_transform,
+    pin_complex_parts,
 ]

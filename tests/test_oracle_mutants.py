@@ -5,6 +5,7 @@ compiled with gcc); the real oracle is never touched.
 """
 import os
 
+import numpy as np
 import pytest
 
 import oracle
@@ -70,3 +71,70 @@ def test_unmutated_copy_passes(tmp_path):
     for pin in oracle_pins.ORACLE_PINS:
         pin(orc)
     assert os.path.exists(so)
+
+
+# Mistakes in the oracle's Python layer (the bit-mask composition and the split
+# complex form), planted on one Oracle instance by replacing a method.
+def _mask_as_one_range(orc):
+    def fwt_mask(x, mask, normalize=True, nthreads=1):
+        if mask == 0:
+            return orc.fwt_bits(x, 0, 0, normalize, nthreads)
+        lo, hi = (mask & -mask).bit_length() - 1, mask.bit_length()
+        return orc.fwt_bits(x, lo, hi - lo, normalize, nthreads)
+    orc.fwt_mask = fwt_mask
+
+
+def _mask_drops_top_run(orc):
+    right = orc.fwt_mask
+
+    def fwt_mask(x, mask, normalize=True, nthreads=1):
+        b = mask.bit_length() - 1
+        while b >= 0 and (mask >> b) & 1:
+            mask &= ~(1 << b)
+            b -= 1
+        return right(x, mask, normalize, nthreads)
+    orc.fwt_mask = fwt_mask
+
+
+def _mask_scales_by_n(orc):
+    right = orc.fwt_mask
+
+    def fwt_mask(x, mask, normalize=True, nthreads=1):
+        y = right(x, mask, False, nthreads)
+        if normalize:
+            n = int(np.asarray(x).shape[-1]).bit_length() - 1
+            y = y * 2.0 ** (-n / 2)
+        return y
+    orc.fwt_mask = fwt_mask
+
+
+def _complex_swaps_parts(orc):
+    def fwt_complex(re, im, normalize=True, nthreads=1):
+        if im is None:
+            return orc.fwt(re, normalize, nthreads), None
+        return orc.fwt(im, normalize, nthreads), orc.fwt(re, normalize, nthreads)
+    orc.fwt_complex = fwt_complex
+
+
+def _complex_imag_from_real(orc):
+    def fwt_complex(re, im, normalize=True, nthreads=1):
+        out = orc.fwt(re, normalize, nthreads)
+        return out, None if im is None else out.copy()
+    orc.fwt_complex = fwt_complex
+
+
+PY_MUTANTS = [_mask_as_one_range, _mask_drops_top_run, _mask_scales_by_n, _complex_swaps_parts,
+              _complex_imag_from_real]
+
+
+@pytest.mark.parametrize("plant", PY_MUTANTS, ids=[m.__name__.strip("_") for m in PY_MUTANTS])
+def test_pins_catch_planted_python_mistake(plant):
+    orc = oracle.Oracle(oracle.build())
+    plant(orc)
+    caught = []
+    for pin in oracle_pins.ORACLE_PINS:
+        try:
+            pin(orc)
+        except AssertionError as e:
+            caught.append((pin.__name__, str(e)))
+    assert caught, f"no pin caught the planted mistake {plant.__name__!r}"
