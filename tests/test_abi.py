@@ -263,3 +263,24 @@ def test_phase_argument_errors_before_launch(lib, fn):
     assert f(a, b, th, 1 << 61, c, d, 4, 3, 1, None) == E        # angle extent overflows
     assert f(a, b, c, 16, c, d, 4, 2, 1, None) == E              # angles overlap re_out
     assert f(None, None, None, 0, None, None, 4, 0, 1, None) == fwt.FWT_OK  # empty batch
+
+
+def test_default_plans_valid_for_every_width_setting(lib):
+    """Whatever column width is set, the default plan of every n and dtype is one the
+    library accepts (re-submitting it through fwt_set_plan validates it on the host)."""
+    try:
+        for dt in ("c32", "c64", "i32"):
+            for cb in (0, 16, 32, 64, 128):
+                fwt.set_column_bytes(dt, cb)
+                for n in range(0, 31):
+                    f = fwt.plan_factors(n, dt)
+                    assert sum(f) == n, (dt, cb, n, f)
+                    if len(f) > 1:
+                        fwt.set_plan(n, dt, f)  # raises FwtError if the plan is invalid
+                        assert fwt.plan_factors(n, dt) == f
+                        fwt.set_plan(n, dt, None)
+    finally:
+        for dt in ("c32", "c64", "i32"):
+            fwt.set_column_bytes(dt, 0)
+            for n in range(0, 31):
+                fwt.set_plan(n, dt, None)
