@@ -65,8 +65,11 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=8,
                     help="vectors per part in the cpu_baseline sample of our arm")
-    ap.add_argument("--ref-sample", type=int, default=1,
-                    help="vectors per part in each step of the reference (CPU oracle) arm")
+    ap.add_argument("--ref-sample", type=int, default=0,
+                    help="vectors per part in each step of the reference (CPU oracle) arm "
+                         "(0 = enough to keep every host core busy)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-configuration measurements (all specified shapes)")
     return ap.parse_args(argv)
 
 
@@ -170,6 +173,88 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(r[0] for r in rows),
                 "sm_max_mhz": max(r[1] for r in rows),
                 "reasons": sorted(reasons), "samples": len(rows)}
+
+
+class NvmlSampler:
+    """The same clock record from NVML (the driver's libnvidia-ml) through ctypes, read
+    every few milliseconds in a thread, so a timed region of ~100 ms still holds tens
+    of samples.  Reads only; changes no setting."""
+
+    # clocks event reason bits (nvml.h)
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
+
+    def __init__(self, gpu_uuid: str, period_s: float = 0.005):
+        import ctypes
+
+        self.period = period_s
+        self.samples = []  # (sm_mhz, sm_max_mhz, reasons bits, power_w)
+        self._stop = threading.Event()
+        self.thread = None
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(gpu_uuid.encode(), ctypes.byref(self.dev)) != 0:
+            raise OSError("no NVML device for " + gpu_uuid)
+        self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        if self._read() is None:
+            raise OSError("NVML clock query failed")
+
+    def _read(self):
+        import ctypes
+
+        sm, mx, pw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(sm)) != 0:  # NVML_CLOCK_SM
+            return None
+        if self.lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx)) != 0:
+            return None
+        if self._reasons(self.dev, ctypes.byref(rs)) != 0:
+            return None
+        power = pw.value / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.dev, ctypes.byref(pw)) == 0 else None
+        return (float(sm.value), float(mx.value), int(rs.value), power)
+
+    def start(self):
+        def run():
+            while not self._stop.is_set():
+                r = self._read()
+                if r is not None:
+                    self.samples.append(r)
+                self._stop.wait(self.period)
+
+        self.thread = threading.Thread(target=run, daemon=True)
+        self.thread.start()
+        time.sleep(0.05)
+
+    def mark(self):
+        return len(self.samples)
+
+    def stop(self):
+        self._stop.set()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, first: int, last: int):
+        rows = self.samples[first:last]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0,
+                    "source": "nvml"}
+        reasons = sorted({name for r in rows for name, bit in self.REASON_BITS.items() if r[2] & bit})
+        powers = [r[3] for r in rows if r[3] is not None]
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": round(max(powers), 1) if powers else None, "source": "nvml, 5 ms"}
+
+
+def clock_sampler(uuid: str):
+    """NVML sampler when the driver library answers, else nvidia-smi at 100 ms."""
+    uid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    try:
+        return NvmlSampler(uid)
+    except (OSError, AttributeError):
+        return ClockSampler(uid)
 
 
 # ---- roofline inputs ---------------------------------------------------------------
@@ -288,7 +373,7 @@ def run_ours(args):
     torch.cuda.synchronize(device)
 
     uuid = str(torch.cuda.get_device_properties(device).uuid)
-    sampler = ClockSampler(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+    sampler = clock_sampler(uuid)
     sampler.start()
     events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * launches_per_step * args.steps)]
     trace = fwt.PassTrace(events)
@@ -385,14 +470,141 @@ def run_ours(args):
     if not args.no_e2e and not args.phase and not args.bits:
         # the host-buffer entry points cover the whole transform only
         result["e2e"] = run_e2e(args, parts, host, device, fwt, world)
+    checks = []
+    if (rank == 0 and world == 1 and not args.no_per_config and args.batch <= 0
+            and bits is None and not args.phase):
+        mine = {w.name: (i, w) for i, w in enumerate(parts)}
+        entries = []
+        for label, name in CONFIGS:
+            w = inputs.WORKLOADS[name]
+            reuse = None
+            if name in mine:  # the step's own buffers (same seeded states)
+                i = mine[name][0]
+                reuse = (dev_in[i], dev_out[i])
+            entry, check = measure_config(label, w, fwt, device, peak, reuse)
+            if reuse is not None:
+                check["host_in"] = host[mine[name][0]]
+            entries.append(entry)
+            checks.append(check)
+        result["per_config"] = entries
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(parts, host, args.cpu_sample)
+        result["cpu_baseline"], errors = cpu_leg(parts, host, args.cpu_sample, checks)
+        for entry in result.get("per_config", []):
+            entry.update(errors.get(entry["config"], {}))
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+# The five specified configurations (the last in fp64 and fp32), in order of n.
+CONFIGS = [("c1", "n10_b64_c32"), ("c2", "n12_b64_c32"), ("c3", "n14_b64_c32"),
+           ("c4", "n18_b256_i32"), ("c5a", "n24_b16_c64"), ("c5b", "n24_b16_c32")]
+
+
+def measure_config(label, w, fwt, device, peak, reuse=None):
+    """Throughput of one specified configuration on its own, inputs in HBM.
+
+    Configurations whose in + out buffers fit in L2 cycle through R copies of them
+    (R x buffers >= 4 x L2, so each transform reads its inputs from HBM); the steps
+    run back to back from a CUDA graph of R transforms (launch overhead stripped;
+    the eager per-step time through the Python binding is reported beside it).
+    Per-kernel device times come from the library's pass trace over eager steps.
+    Returns the entry and, for the CPU leg's oracle check, the inputs and the GPU
+    results of the vectors it checks."""
+    import numpy as np
+    import torch
+
+    l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 128 << 20))
+    set_bytes = 2 * w.bytes_in  # inputs and outputs
+    reps = 1 if set_bytes >= l2 else -(-4 * l2 // set_bytes)
+    if reuse is not None:
+        (a, b), (c, d) = reuse
+        host_in = None
+    else:
+        host_in = w.generate()
+        a = torch.from_numpy(host_in[0]).to(device)
+        b = torch.from_numpy(host_in[1]).to(device)
+        c, d = torch.empty_like(a), torch.empty_like(b)
+    sets = [((a, b), (c, d))]
+    for _ in range(reps - 1):
+        sets.append(((a.clone(), b.clone()), (torch.empty_like(a), torch.empty_like(b))))
+
+    def step(r):
+        (x, y), (u, v) = sets[r]
+        fwt.transform(x, y, u, v, normalize=w.normalize)
+
+    for r in range(min(reps, 3)):
+        step(r)
+    torch.cuda.synchronize(device)
+    small = set_bytes < l2
+    names = pass_names(w, fwt)
+    npass = len(names)
+    # per-kernel device times, eager launches under the pass trace
+    k_eager = max(reps, 300) if small else 20
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * npass * k_eager)]
+    trace = fwt.PassTrace(events)
+    with trace:
+        for i in range(k_eager):
+            step(i % reps)
+    torch.cuda.synchronize(device)
+    durs = trace.durations_ms()
+    kernels = []
+    algo = 2 * w.bytes_in  # every pass reads and writes the whole batch once
+    for li, nm in enumerate(names):
+        ds = durs[li::npass]
+        mean = statistics.mean(ds)
+        kernels.append({"kernel": nm, "mean_us": round(mean * 1e3, 2),
+                        "median_us": round(statistics.median(ds) * 1e3, 2),
+                        "min_us": round(min(ds) * 1e3, 2),
+                        "gbs": round(algo / (mean * 1e-3) / 1e9, 1)})
+    # eager steps through the Python binding (host launch overhead included)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(k_eager):
+        step(i % reps)
+    e1.record()
+    torch.cuda.synchronize(device)
+    eager_us = e0.elapsed_time(e1) * 1e3 / k_eager
+    # back-to-back steps from a CUDA graph
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(device)
+    with torch.cuda.graph(graph, stream=side):
+        for r in range(reps):
+            step(r)
+    replays = max(1, -(-3000 // reps)) if small else 20
+    graph.replay()
+    torch.cuda.synchronize(device)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record()
+    for _ in range(replays):
+        graph.replay()
+    g1.record()
+    torch.cuda.synchronize(device)
+    steps = replays * reps
+    step_s = g0.elapsed_time(g1) / 1e3 / steps
+    gbs = algo / step_s / 1e9
+    entry = {
+        "config": label, "workload": w.name, "n": w.n, "batch": w.batch, "dtype": w.dtype,
+        "normalize": w.normalize, "factors": fwt.plan_factors(w.n, w.dtype), "passes": npass,
+        "vectors_per_s": round(w.batch / step_s, 1), "us_per_step": round(step_s * 1e6, 3),
+        "effective_gbs": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+        "algo_bytes_per_step": algo,
+        "timing": ("CUDA graph of %d back-to-back transforms over %d buffer sets (%.0f MiB, "
+                   "inputs read from HBM), replayed %d times" % (reps, reps, reps * set_bytes / 2 ** 20, replays)
+                   if small else "CUDA graph of one transform, replayed %d times (inputs larger than L2)" % replays),
+        "eager_us_per_step": round(eager_us, 3),
+        "kernels": kernels,
+    }
+    # the vectors the CPU leg checks against the oracle: all of them up to n = 18, the
+    # first and the last at n = 24
+    rows = list(range(w.batch)) if w.n <= 18 else [0, w.batch - 1]
+    got = (c[rows].cpu().numpy(), d[rows].cpu().numpy())
+    check = {"label": label, "workload": w, "rows": rows, "host_in": host_in, "got": got}
+    del sets
+    return entry, check
 
 
 def run_e2e(args, parts, host, device, fwt, world):
@@ -456,20 +668,95 @@ def oracle_step(orc, parts, host, threads):
     return min(threads, sum(min(per_job, arr.shape[0]) for arr, _ in jobs))
 
 
+def cpu_info():
+    """Host core count and CPU model (lscpu, else /proc/cpuinfo)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+        arch = next((ln.split(":", 1)[1].strip() for ln in out.splitlines()
+                     if ln.startswith("Architecture:")), None)
+        if model and arch:
+            model = f"{model} ({arch})"
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except OSError:
+            pass
+    return {"nproc": os.cpu_count() or 1, "model": model or "unknown"}
+
+
 def cpu_baseline(parts, host, sample):
-    """The CPU oracle as it stands, on the first `sample` vectors of each part."""
+    """The CPU oracle as it stands, timed twice on the host: one thread on the first
+    vector of each part, and every core on the first `sample` vectors of each part
+    (the arrays run concurrently, each split over whole vectors)."""
     import oracle
 
     orc = oracle.default()
-    threads = max(1, os.cpu_count() or 1)
+    info = cpu_info()
+    threads = max(1, info["nproc"])
+    one = [(re[:1], im[:1]) for re, im in host]
+    t = time.perf_counter()
+    for w, (re, im) in zip(parts, one):
+        for arr in (re, im):
+            orc.fwt(arr, normalize=w.normalize, nthreads=1)
+    secs1 = time.perf_counter() - t
+    v1 = sum(min(1, w.batch) for w in parts)
     cut = [(re[:sample], im[:sample]) for re, im in host]
     t = time.perf_counter()
     used = oracle_step(orc, parts, cut, threads)
     secs = time.perf_counter() - t
     vectors = sum(min(sample, w.batch) for w in parts)
+    names = ", ".join(w.name for w in parts)
     return {"value": round(vectors / secs, 4), "unit": UNIT, "cores": used, "kind": "oracle",
             "sample": "first %d vectors of each part (%s), %.1f s wall on %d threads" % (
-                sample, ", ".join(w.name for w in parts), secs, used)}
+                sample, names, secs, used),
+            "single_thread": {"value": round(v1 / secs1, 4), "unit": UNIT, "cores": 1,
+                              "sample": "first vector of each part (%s), %.1f s wall" % (names, secs1)},
+            "all_cores": {"value": round(vectors / secs, 4), "unit": UNIT, "cores": used},
+            "nproc": info["nproc"], "cpu_model": info["model"]}
+
+
+def cpu_leg(parts, host, sample, checks):
+    """The CPU oracle's leg of the run: its timed baseline, then the check of the
+    per-configuration GPU results it was handed against the oracle (per-vector
+    complex relative L2 error, max over the checked vectors; int32 bit for bit)."""
+    import numpy as np
+
+    import oracle
+
+    base = cpu_baseline(parts, host, sample)
+    threads = max(1, os.cpu_count() or 1)
+    errors = {}
+    for ch in checks:
+        w, rows = ch["workload"], ch["rows"]
+        re, im = ch["host_in"]
+        ore, oim = oracle.fwt_complex(re[rows], im[rows], normalize=w.normalize, nthreads=threads)
+        gre, gim = ch["got"]
+        desc = "all %d vectors" % w.batch if len(rows) == w.batch else "vectors %s" % rows
+        if w.dtype == "i32":
+            errors[ch["label"]] = {"oracle_check": desc, "bit_exact": bool(
+                np.array_equal(gre, ore) and np.array_equal(gim, oim))}
+            continue
+        worst = 0.0
+        for k in range(len(rows)):
+            ref = np.concatenate([ore[k], oim[k]])
+            got = np.concatenate([gre[k], gim[k]]).astype(np.float64)
+            scale = max(float(np.max(np.abs(ref))), 1e-300)
+            num = float(np.linalg.norm((got - ref) / scale))
+            den = float(np.linalg.norm(ref / scale)) or 1.0
+            worst = max(worst, num / den)
+        errors[ch["label"]] = {"oracle_check": desc, "max_rel_l2_err": float("%.3e" % worst),
+                               "tolerance": 2e-6 if w.dtype == "c32" else 1e-12}
+    return base, errors
 
 
 # ---- the reference arm: the CPU oracle -------------------------------------------------
@@ -482,9 +769,13 @@ def run_reference(args):
     from walsh_hadamard_transform_gb300 import inputs
 
     parts = [inputs.WORKLOADS[name] for name in STEP_WORKLOADS[args.workload]]
-    sample = max(1, min(args.ref_sample, min(w.batch for w in parts)))
+    info = cpu_info()
+    threads = max(1, info["nproc"])
+    # each step runs the 2 arrays of every part at once, each over its vectors: enough
+    # vectors that every core has one
+    want = args.ref_sample if args.ref_sample > 0 else -(-threads // (2 * len(parts)))
+    sample = max(1, min(want, min(w.batch for w in parts)))
     host = [w.generate(batch=sample) for w in parts]
-    threads = max(1, os.cpu_count() or 1)
     orc = oracle.default()
     for _ in range(args.warmup):
         oracle_step(orc, parts, host, threads)
@@ -503,7 +794,7 @@ def run_reference(args):
         "data": "synthetic (seeded PCG64)",
         "config": {"workload": args.workload, "sample": desc},
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": used, "kind": "oracle",
-                         "sample": desc},
+                         "sample": desc, "nproc": info["nproc"], "cpu_model": info["model"]},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

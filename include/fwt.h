@@ -212,18 +212,34 @@ int fwt_host_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, in
 size_t fwt_host_workspace_bytes(int dtype, int n, int64_t batch, int with_im);
 
 /*
- * fwt_host_* without a caller workspace: the staging buffer is the library's own
- * static device memory, a file-scope __device__ array of
- * fwt_host_static_workspace_bytes() bytes per device that is part of the module
- * image (set up with cudaGetSymbolAddress on first use on a device), so nothing is
- * allocated at run time.  The array occupies that much device memory once its
- * module is loaded: at the first call under CUDA's lazy module loading (the
- * default), at context creation under eager loading.  The pages have no counterpart of this entry point: it is
- * a convenience of the host-buffer path.  Same operation, arguments, layout,
- * in-place rules, asynchrony and errors as fwt_host_*; a vector (both parts) larger
- * than the static buffer is FWT_ERR_INVALID_ARG.  Calls share the buffer: each call
- * makes `stream` wait until the previous call (any stream, same device) has copied
- * its last chunk out.
+ * fwt_host_* without a caller workspace, for callers that cannot allocate device
+ * memory: a plug-in or library running inside a host application that owns the
+ * device memory (its own pool, or a fixed budget set at start-up) and forbids
+ * stray cudaMalloc calls, or a latency-bound loop that cannot afford cudaMalloc's
+ * implicit device synchronisation.  The pages have no counterpart of this entry
+ * point: it is a convenience of the host-buffer path.
+ *
+ * The staging buffer is the library's own static device memory: a file-scope
+ * __device__ array of fwt_host_static_workspace_bytes() bytes (512 MiB) that is
+ * part of the module image, so nothing is allocated at run time (no cudaMalloc,
+ * cudaFree or allocating library call).  Every device that loads the module holds
+ * the array until the process exits: from the first call under CUDA's lazy module
+ * loading (the default), from context creation under eager loading.
+ *
+ * The first call on a device does a one-time set-up with that device current: it
+ * looks up the array's device address (cudaGetSymbolAddress) and creates an event.
+ * Make that first call before any stream capture.  The address and the event are
+ * kept for the life of the process: they, like the copy streams of fwt_host_*, do
+ * not survive cudaDeviceReset or the destruction of the device's primary context.
+ *
+ * Same operation, arguments, layout, in-place rules, asynchrony and errors as
+ * fwt_host_*.  Every argument error is returned before any CUDA call; in
+ * particular a vector (both parts) larger than the static buffer is
+ * FWT_ERR_INVALID_ARG.  Calls share the buffer, which keeps the last call's staged
+ * data (every call overwrites what it reads before reading it).  Calls in one
+ * process do not overlap on the GPU: each call makes `stream` wait until the
+ * previous call (any stream, same device) has copied its last chunk out, also when
+ * that call failed part-way.
  */
 int fwt_host_static_c32(const float* re_in, const float* im_in, float* re_out, float* im_out,
                         int n, int64_t batch, int normalize, fwt_stream_t stream);

@@ -8,6 +8,7 @@
 #include <cstdlib>
 #include <atomic>
 #include <mutex>
+#include <unordered_map>
 #include <vector>
 
 #include <cuda_runtime.h>
@@ -39,15 +40,31 @@ const std::vector<KernelEntry>& table() {
   return t;
 }
 
-// Column kernels are also keyed by segment width and mover; cluster kernels by
-// their slice size (passed as col_bytes).
+// Kernels are found by (dtype, kind, K), column kernels also by segment width and
+// mover, cluster kernels by their slice size (passed as col_bytes).  A planned call
+// looks up tens of kernels, so the table is indexed once by that key.
+uint64_t kernel_key(int dtype, int kind, int K, int col_bytes, int tma) {
+  return (uint64_t)(uint32_t)dtype << 48 | (uint64_t)(uint32_t)kind << 40 |
+         (uint64_t)(uint32_t)K << 32 | (uint64_t)(uint32_t)col_bytes << 8 | (uint64_t)(tma & 0xff);
+}
+uint64_t entry_key(const KernelEntry& e) {
+  return kernel_key(e.dtype, e.kind, e.K, e.kind == KIND_COL ? e.col_bytes : e.kind == KIND_CLUSTER ? e.TB : 0,
+                    e.kind == KIND_COL ? e.tma : 0);
+}
+const std::unordered_map<uint64_t, const KernelEntry*>& kernel_index() {
+  static const std::unordered_map<uint64_t, const KernelEntry*> ix = [] {
+    std::unordered_map<uint64_t, const KernelEntry*> m;
+    for (const KernelEntry& e : table()) m.emplace(entry_key(e), &e);  // first entry wins
+    return m;
+  }();
+  return ix;
+}
 const KernelEntry* find_kernel(int dtype, int kind, int K, int col_bytes = 0, int tma = 0) {
-  for (const KernelEntry& e : table())
-    if (e.dtype == dtype && e.kind == kind && e.K == K &&
-        (kind != KIND_COL || (e.col_bytes == col_bytes && e.tma == tma)) &&
-        (kind != KIND_CLUSTER || e.TB == col_bytes))
-      return &e;
-  return nullptr;
+  const auto& ix = kernel_index();
+  const auto it = ix.find(kernel_key(dtype, kind, K,
+                                     kind == KIND_COL || kind == KIND_CLUSTER ? col_bytes : 0,
+                                     kind == KIND_COL ? tma : 0));
+  return it == ix.end() ? nullptr : it->second;
 }
 
 int elem_size(int dtype) { return dtype == FWT_C64 ? 8 : 4; }
@@ -1069,6 +1086,20 @@ int fwt_trace_count(void) { return fwt::g_trace_count; }
 int fwt_selfcheck(void) {
   int fails = 0;
   for (const fwt::KernelEntry& e : fwt::table()) fails += e.selfcheck();
+  // the kernel index returns, for every entry's key, the first table entry with it
+  for (const fwt::KernelEntry& e : fwt::table()) {
+    const int cb = e.kind == fwt::KIND_COL ? e.col_bytes : e.kind == fwt::KIND_CLUSTER ? e.TB : 0;
+    const fwt::KernelEntry* first = nullptr;
+    for (const fwt::KernelEntry& f : fwt::table())
+      if (fwt::entry_key(f) == fwt::entry_key(e)) {
+        first = &f;
+        break;
+      }
+    if (fwt::find_kernel(e.dtype, e.kind, e.K, cb, e.tma) != first) {
+      fprintf(stderr, "fwt_selfcheck: kernel index disagrees with the table\n");
+      ++fails;
+    }
+  }
   for (int dt = 0; dt < 3; ++dt)
     for (int n = 0; n <= 30; ++n)
       if (!fwt::plan_valid(n, dt, fwt::default_plan(n, dt))) {

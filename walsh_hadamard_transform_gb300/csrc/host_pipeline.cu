@@ -31,6 +31,7 @@ struct DeviceStreams {
   bool ready = false;
   cudaStream_t in = nullptr, out = nullptr;
   cudaEvent_t start = nullptr;
+  cudaEvent_t joined_in = nullptr, joined_out = nullptr;  // error path: copy streams -> caller
   cudaEvent_t loaded[kSlots] = {}, done[kSlots] = {}, drained[kSlots] = {};
 };
 
@@ -47,6 +48,8 @@ cudaError_t streams_for_current_device(DeviceStreams*& ds) {
   err = cudaStreamCreateWithFlags(&ds->in, cudaStreamNonBlocking);
   if (err == cudaSuccess) err = cudaStreamCreateWithFlags(&ds->out, cudaStreamNonBlocking);
   if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ds->start, cudaEventDisableTiming);
+  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ds->joined_in, cudaEventDisableTiming);
+  if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ds->joined_out, cudaEventDisableTiming);
   for (int s = 0; s < kSlots && err == cudaSuccess; ++s) {
     err = cudaEventCreateWithFlags(&ds->loaded[s], cudaEventDisableTiming);
     if (err == cudaSuccess) err = cudaEventCreateWithFlags(&ds->done[s], cudaEventDisableTiming);
@@ -71,19 +74,32 @@ int64_t target_chunk(int esz, int n, int64_t batch, int parts) {
   return std::max<int64_t>(1, std::min(c, batch));
 }
 
-int run_host(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out, int n,
-             int64_t batch, int normalize, void* workspace, size_t workspace_bytes,
-             cudaStream_t stream) {
+// How a call's batch is cut into chunks and slots, from its arguments alone.
+struct HostPlan {
+  int esz = 4;
+  bool has_im = false;
+  int64_t c = 0;        // vectors per chunk
+  size_t sb = 0;        // bytes of one slot (both parts)
+  size_t part_off = 0;  // offset of the imaginary part within a slot
+  int slots = 0;
+};
+
+// Every argument check of a host-buffer call, before any CUDA call: sizes, the
+// pointers (the workspace pointer itself is checked by the caller), overlapping
+// host arrays, and whether one vector fits `workspace_bytes`.  FWT_OK with
+// batch == 0 means there is nothing to do.
+int validate_host(int dtype, const void* re_in, const void* im_in, const void* re_out,
+                  const void* im_out, int n, int64_t batch, int normalize,
+                  size_t workspace_bytes, HostPlan& hp) {
   if (n < 0 || n > 30 || batch < 0) return FWT_ERR_INVALID_ARG;
   if (batch == 0) return FWT_OK;
   const int esz = dtype == FWT_C64 ? 8 : 4;
   if (batch > (INT64_MAX >> n) / esz) return FWT_ERR_INVALID_ARG;
-  if (!re_in || !re_out || !workspace) return FWT_ERR_INVALID_ARG;
+  if (!re_in || !re_out) return FWT_ERR_INVALID_ARG;
   const bool has_im = im_in || im_out;
   if (has_im && (!im_in || !im_out)) return FWT_ERR_INVALID_ARG;
   if (!has_im && dtype != FWT_I32) return FWT_ERR_INVALID_ARG;
   if (dtype == FWT_I32 && normalize) return FWT_ERR_UNSUPPORTED;
-  if ((uintptr_t)workspace & 15u) return FWT_ERR_MISALIGNED;
   const size_t bytes = (size_t)(batch << n) * (size_t)esz;
   // host outputs may coincide exactly with their own input, and with nothing else
   auto disjoint = [bytes](const void* a, const void* b) {
@@ -102,29 +118,59 @@ int run_host(int dtype, const void* re_in, const void* im_in, void* re_out, void
   const size_t sb = slot_bytes(esz, n, c, parts);
   const int slots = (int)std::min<size_t>(kSlots, workspace_bytes / sb);
   if (slots < 1) return FWT_ERR_INVALID_ARG;  // not even one vector fits
-  const size_t part_off = align_up((size_t)(c << n) * (size_t)esz);
+  hp.esz = esz;
+  hp.has_im = has_im;
+  hp.c = c;
+  hp.sb = sb;
+  hp.part_off = align_up((size_t)(c << n) * (size_t)esz);
+  hp.slots = slots;
+  return FWT_OK;
+}
 
+// Enqueues the pipeline of a validated call (batch > 0).  `started` becomes true
+// once anything has been enqueued.  On a failure after that, the two copy streams
+// are joined back into `stream` (best effort), so that work the caller enqueues on
+// `stream` afterwards still comes after every copy this call enqueued.
+int enqueue_host(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out,
+                 int n, int64_t batch, int normalize, void* workspace, const HostPlan& hp,
+                 cudaStream_t stream, bool& started) {
+  started = false;
+  const int esz = hp.esz;
+  const bool has_im = hp.has_im;
+  const int64_t c = hp.c;
+  const int slots = hp.slots;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceStreams* ds = nullptr;
   cudaError_t err = streams_for_current_device(ds);
-  auto fail = [&](cudaError_t e) {
-    set_last_cuda_error((int)e);
+  if (err != cudaSuccess) {
+    set_last_cuda_error((int)err);
     return FWT_ERR_CUDA;
+  }
+  auto fail = [&](int status, cudaError_t e) {
+    if (status == FWT_ERR_CUDA) set_last_cuda_error((int)e);
+    if (started) {
+      if (cudaEventRecord(ds->joined_in, ds->in) == cudaSuccess)
+        cudaStreamWaitEvent(stream, ds->joined_in, 0);
+      if (cudaEventRecord(ds->joined_out, ds->out) == cudaSuccess)
+        cudaStreamWaitEvent(stream, ds->joined_out, 0);
+    }
+    return status;
   };
-  if (err != cudaSuccess) return fail(err);
   // nothing starts before the work the caller enqueued on `stream` so far
   err = cudaEventRecord(ds->start, stream);
-  if (err == cudaSuccess) err = cudaStreamWaitEvent(ds->in, ds->start, 0);
+  if (err != cudaSuccess) return fail(FWT_ERR_CUDA, err);
+  started = true;
+  err = cudaStreamWaitEvent(ds->in, ds->start, 0);
   if (err == cudaSuccess) err = cudaStreamWaitEvent(ds->out, ds->start, 0);
-  if (err != cudaSuccess) return fail(err);
+  if (err != cudaSuccess) return fail(FWT_ERR_CUDA, err);
 
   const int64_t chunks = (batch + c - 1) / c;
   for (int64_t k = 0; k < chunks; ++k) {
     const int s = (int)(k % slots);
     const int64_t v0 = k * c, nv = std::min(c, batch - v0);
     const size_t off = (size_t)(v0 << n) * (size_t)esz, len = (size_t)(nv << n) * (size_t)esz;
-    char* d_re = (char*)workspace + (size_t)s * sb;
-    char* d_im = has_im ? d_re + part_off : nullptr;
+    char* d_re = (char*)workspace + (size_t)s * hp.sb;
+    char* d_im = has_im ? d_re + hp.part_off : nullptr;
     // copy in, once the slot's previous chunk has been copied out
     if (k >= slots) err = cudaStreamWaitEvent(ds->in, ds->drained[s], 0);
     if (err == cudaSuccess)
@@ -133,7 +179,7 @@ int run_host(int dtype, const void* re_in, const void* im_in, void* re_out, void
       err = cudaMemcpyAsync(d_im, (const char*)im_in + off, len, cudaMemcpyHostToDevice, ds->in);
     if (err == cudaSuccess) err = cudaEventRecord(ds->loaded[s], ds->in);
     if (err == cudaSuccess) err = cudaStreamWaitEvent(stream, ds->loaded[s], 0);
-    if (err != cudaSuccess) return fail(err);
+    if (err != cudaSuccess) return fail(FWT_ERR_CUDA, err);
     // transform in place on the caller's stream
     int st;
     if (dtype == FWT_C32)
@@ -145,7 +191,7 @@ int run_host(int dtype, const void* re_in, const void* im_in, void* re_out, void
     else
       st = fwt_batched_i32((const int32_t*)d_re, (const int32_t*)d_im, (int32_t*)d_re,
                            (int32_t*)d_im, n, nv, 0, stream);
-    if (st != FWT_OK) return st;
+    if (st != FWT_OK) return fail(st, cudaSuccess);  // the transform recorded its own error
     err = cudaEventRecord(ds->done[s], stream);
     // copy out
     if (err == cudaSuccess) err = cudaStreamWaitEvent(ds->out, ds->done[s], 0);
@@ -154,11 +200,25 @@ int run_host(int dtype, const void* re_in, const void* im_in, void* re_out, void
     if (err == cudaSuccess && has_im)
       err = cudaMemcpyAsync((char*)im_out + off, d_im, len, cudaMemcpyDeviceToHost, ds->out);
     if (err == cudaSuccess) err = cudaEventRecord(ds->drained[s], ds->out);
-    if (err != cudaSuccess) return fail(err);
+    if (err != cudaSuccess) return fail(FWT_ERR_CUDA, err);
   }
   // the caller's stream reaches this point only after the last copy out
   err = cudaStreamWaitEvent(stream, ds->drained[(chunks - 1) % slots], 0);
-  return err == cudaSuccess ? FWT_OK : fail(err);
+  return err == cudaSuccess ? FWT_OK : fail(FWT_ERR_CUDA, err);
+}
+
+int run_host(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out, int n,
+             int64_t batch, int normalize, void* workspace, size_t workspace_bytes,
+             cudaStream_t stream) {
+  HostPlan hp;
+  int st = validate_host(dtype, re_in, im_in, re_out, im_out, n, batch, normalize,
+                         workspace_bytes, hp);
+  if (st != FWT_OK || batch == 0) return st;
+  if (!workspace) return FWT_ERR_INVALID_ARG;
+  if ((uintptr_t)workspace & 15u) return FWT_ERR_MISALIGNED;
+  bool started = false;
+  return enqueue_host(dtype, re_in, im_in, re_out, im_out, n, batch, normalize, workspace, hp,
+                      stream, started);
 }
 
 }  // namespace
@@ -203,7 +263,9 @@ int fwt_host_i32(const int32_t* re_in, const int32_t* im_in, int32_t* re_out, in
 // device array (allocated with the module when it loads, one per device), found with
 // cudaGetSymbolAddress.  The library allocates nothing at run time.  Calls share the
 // buffer, so each one first waits (on the caller's stream) for the previous one to
-// have copied its last chunk out.
+// have copied its last chunk out.  The buffer's address and that event are looked up
+// once per device and kept: they do not survive cudaDeviceReset or the destruction
+// of the device's primary context (nor do the copy streams above).
 namespace fwt {
 namespace {
 
@@ -220,18 +282,18 @@ std::vector<StaticWorkspace> g_static;
 
 int run_host_static(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_out,
                     int n, int64_t batch, int normalize, cudaStream_t stream) {
-  // argument errors before any CUDA call (the pipeline repeats the full checks)
-  if (n < 0 || n > 30 || batch < 0) return FWT_ERR_INVALID_ARG;
-  if (batch == 0) return FWT_OK;
-  if (!re_in || !re_out || (!im_in) != (!im_out)) return FWT_ERR_INVALID_ARG;
-  if (!im_in && dtype != FWT_I32) return FWT_ERR_INVALID_ARG;
-  if (dtype == FWT_I32 && normalize) return FWT_ERR_UNSUPPORTED;
+  // every argument error (a vector too large for the static buffer included) comes
+  // back before any CUDA call
+  HostPlan hp;
+  int st = validate_host(dtype, re_in, im_in, re_out, im_out, n, batch, normalize,
+                         kStaticWorkspaceBytes, hp);
+  if (st != FWT_OK || batch == 0) return st;
   std::lock_guard<std::mutex> lock(g_static_mu);
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err == cudaSuccess && (int)g_static.size() <= dev) g_static.resize(dev + 1);
   StaticWorkspace* sw = err == cudaSuccess ? &g_static[dev] : nullptr;
-  if (err == cudaSuccess && !sw->ptr) {
+  if (err == cudaSuccess && !sw->ptr) {  // first call on this device
     err = cudaGetSymbolAddress(&sw->ptr, g_static_workspace);
     if (err == cudaSuccess) err = cudaEventCreateWithFlags(&sw->done, cudaEventDisableTiming);
     if (err != cudaSuccess) sw->ptr = nullptr;
@@ -241,16 +303,21 @@ int run_host_static(int dtype, const void* re_in, const void* im_in, void* re_ou
     set_last_cuda_error((int)err);
     return FWT_ERR_CUDA;
   }
-  const int st = run_host(dtype, re_in, im_in, re_out, im_out, n, batch, normalize, sw->ptr,
-                          kStaticWorkspaceBytes, stream);
-  if (st != FWT_OK) return st;
-  err = cudaEventRecord(sw->done, stream);
-  if (err != cudaSuccess) {
-    set_last_cuda_error((int)err);
-    return FWT_ERR_CUDA;
+  bool started = false;
+  st = enqueue_host(dtype, re_in, im_in, re_out, im_out, n, batch, normalize, sw->ptr, hp, stream,
+                    started);
+  // Once anything was enqueued, the next call must wait for it even when this one
+  // failed part-way: the failed call's copies were joined back into `stream`.
+  if (started) {
+    err = cudaEventRecord(sw->done, stream);
+    if (err == cudaSuccess) {
+      sw->used = true;
+    } else if (st == FWT_OK) {
+      set_last_cuda_error((int)err);
+      st = FWT_ERR_CUDA;
+    }
   }
-  sw->used = true;
-  return FWT_OK;
+  return st;
 }
 
 }  // namespace

@@ -13,6 +13,11 @@ Recipe (the source pages give the shapes, not the generator):
 * fp32 workloads are the float64 draw rounded once to float32.
 * int32 workloads: ``integers(-8, 9, (batch, N))`` (uniform on -8..8 inclusive),
   imaginary part all zero.
+
+Edge-case recipes (``edge_pair``), for tests only: full-range int32 (every
+intermediate wraps), and fp64 inputs that drive a fixed-point conversion to its
+worst case (one-signed values with full mantissas; every element just below a
+power of two; one large entry per tile with full-mantissa entries far below it).
 """
 from __future__ import annotations
 
@@ -94,3 +99,41 @@ def random_pair(n: int, batch: int, dtype: str, seed: int):
     if dtype == "i32":
         return draw("uniform_int8", n, batch, seed, dtype)
     return draw("gaussian", n, batch, seed, dtype)
+
+
+def edge_pair(kind: str, n: int, batch: int, seed: int, tile_bits: int = 13):
+    """Seeded (re, im) pair of (batch, 2^n) edge-case arrays:
+
+    * ``"int32_full"``: int32 uniform over the whole range [-2^31, 2^31), both parts.
+    * ``"fp64_one_signed"``: fp64 uniform in [1, 2) (full 52-bit mantissas), both parts.
+    * ``"fp64_below_pow2"``: every element nextafter(2^e, 0) for a per-vector e in
+      [-20, 20) (all 53 significand bits set); the imaginary part negated.
+    * ``"fp64_spike"``: per block of 2^tile_bits contiguous elements one entry of
+      magnitude 2^e (e per vector in [-20, 20)), the others full-mantissa values in
+      [1, 2) * 2^(e - 30); signs random.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    N = 1 << n
+    if kind == "int32_full":
+        z = rng.integers(-(1 << 31), 1 << 31, size=(batch, 2, N), dtype=np.int64).astype(np.int32)
+        return np.ascontiguousarray(z[:, 0]), np.ascontiguousarray(z[:, 1])
+    e = rng.integers(-20, 20, size=batch)
+    if kind == "fp64_one_signed":
+        z = 1.0 + rng.random((batch, 2, N))
+    elif kind == "fp64_below_pow2":
+        v = np.nextafter(np.ldexp(1.0, e), 0.0)
+        z = np.empty((batch, 2, N))
+        z[:, 0] = v[:, None]
+        z[:, 1] = -v[:, None]
+    elif kind == "fp64_spike":
+        z = np.ldexp(1.0 + rng.random((batch, 2, N)), (e - 30)[:, None, None])
+        tb = min(tile_bits, n)
+        blocks = N >> tb
+        pos = rng.integers(0, 1 << tb, size=(batch, 2, blocks)) + (np.arange(blocks) << tb)
+        for b in range(batch):
+            for c in range(2):
+                z[b, c, pos[b, c]] = np.ldexp(1.0, int(e[b]))
+        z *= rng.choice([-1.0, 1.0], size=z.shape)
+    else:
+        raise ValueError(f"unknown edge-case recipe {kind!r}")
+    return np.ascontiguousarray(z[:, 0]), np.ascontiguousarray(z[:, 1])
