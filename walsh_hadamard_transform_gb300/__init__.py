@@ -98,6 +98,10 @@ def library() -> ctypes.CDLL:
         lib.fwt_set_tma.restype = ci
         lib.fwt_get_tma.argtypes = []
         lib.fwt_get_tma.restype = ci
+        lib.fwt_set_pdl.argtypes = [ci]
+        lib.fwt_set_pdl.restype = ci
+        lib.fwt_get_pdl.argtypes = []
+        lib.fwt_get_pdl.restype = ci
         lib.fwt_set_cluster.argtypes = [ci]
         lib.fwt_set_cluster.restype = ci
         lib.fwt_get_cluster.argtypes = []
@@ -312,6 +316,19 @@ def tma() -> int:
     return library().fwt_get_tma()
 
 
+def set_pdl(mode: int) -> None:
+    """Launch pass kernels with programmatic stream serialisation (1, the default:
+    a kernel may be scheduled while the previous one on the stream finishes, and
+    waits for it before touching memory) or plainly (0); results are identical."""
+    st = library().fwt_set_pdl(int(mode))
+    if st != FWT_OK:
+        raise FwtError(st, f"fwt_set_pdl({mode})")
+
+
+def pdl() -> int:
+    return library().fwt_get_pdl()
+
+
 CLUSTER_NEVER, CLUSTER_AUTO, CLUSTER_FROM_14 = 0, 1, 2
 
 
@@ -398,13 +415,47 @@ _HOST_ENTRY = {"c32": fwt_host_c32, "c64": fwt_host_c64, "i32": fwt_host_i32}
 _MASK_ENTRY = {"c32": fwt_mask_c32, "c64": fwt_mask_c64, "i32": fwt_mask_i32}
 
 
-def _dtype_key(t) -> str:
-    import torch
+_torch = None
+_DTYPE_KEYS = None
 
-    key = {torch.float32: "c32", torch.float64: "c64", torch.int32: "i32"}.get(t.dtype)
+
+def _torch_mod():
+    global _torch, _DTYPE_KEYS
+    if _torch is None:
+        import torch
+
+        _DTYPE_KEYS = {torch.float32: "c32", torch.float64: "c64", torch.int32: "i32"}
+        _torch = torch
+    return _torch
+
+
+def _dtype_key(t) -> str:
+    _torch_mod()
+    key = _DTYPE_KEYS.get(t.dtype)
     if key is None:
         raise TypeError(f"unsupported dtype {t.dtype}: use float32, float64 or int32")
     return key
+
+
+def _stream_handle(stream, device):
+    """The raw cudaStream_t of ``stream`` (default: the current PyTorch stream of
+    ``device``)."""
+    if stream is not None:
+        return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    torch = _torch_mod()
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(device.index)
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _on_device(device, call):
+    """Runs ``call`` with ``device`` current (switching only when it is not)."""
+    torch = _torch_mod()
+    if device.index == torch.cuda.current_device():
+        return call()
+    with torch.cuda.device(device):
+        return call()
 
 
 def transform(re, im=None, out_re=None, out_im=None, normalize: bool = True, stream=None,
@@ -419,8 +470,7 @@ def transform(re, im=None, out_re=None, out_im=None, normalize: bool = True, str
     (an int below 2^n) transforms the index bits set in it.  Returns
     (out_re, out_im).
     """
-    import torch
-
+    torch = _torch_mod()
     key = _dtype_key(re)
     if not re.is_cuda:
         raise ValueError("transform() needs CUDA tensors; use transform_host() for host arrays")
@@ -430,31 +480,31 @@ def transform(re, im=None, out_re=None, out_im=None, normalize: bool = True, str
     n = int(N).bit_length() - 1
     if N < 1 or (1 << n) != N:
         raise ValueError(f"row length {N} is not a power of two")
+    if bits is not None and mask is not None:
+        raise ValueError("give bits or mask, not both")
     if out_re is None:
         out_re = torch.empty_like(re)
     if im is not None and out_im is None:
         out_im = torch.empty_like(im)
+    dtype, shape, device = re.dtype, re.shape, re.device
     for t in (re, im, out_re, out_im):
         if t is None:
             continue
-        if t.dtype != re.dtype or t.shape != re.shape or t.device != re.device:
+        if t.dtype != dtype or t.shape != shape or t.device != device:
             raise ValueError("re, im and outputs must share dtype, shape and device")
         if not t.is_contiguous():
             raise ValueError("tensors must be contiguous")
-    if stream is None:
-        stream = torch.cuda.current_stream(re.device)
-    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    handle = _stream_handle(stream, device)
     ptrs = (re.data_ptr(), im.data_ptr() if im is not None else None, out_re.data_ptr(),
             out_im.data_ptr() if out_im is not None else None)
-    with torch.cuda.device(re.device):
-        if bits is not None and mask is not None:
-            raise ValueError("give bits or mask, not both")
-        if mask is not None:
-            st = _MASK_ENTRY[key](*ptrs, n, batch, int(mask), normalize, handle)
-        elif bits is None:
-            st = _ENTRY[key](*ptrs, n, batch, normalize, handle)
-        else:
-            st = _BITS_ENTRY[key](*ptrs, n, batch, int(bits[0]), int(bits[1]), normalize, handle)
+    if mask is not None:
+        call = lambda: _MASK_ENTRY[key](*ptrs, n, batch, int(mask), normalize, handle)  # noqa: E731
+    elif bits is None:
+        call = lambda: _ENTRY[key](*ptrs, n, batch, normalize, handle)  # noqa: E731
+    else:
+        call = lambda: _BITS_ENTRY[key](*ptrs, n, batch, int(bits[0]), int(bits[1]),  # noqa: E731
+                                        normalize, handle)
+    st = _on_device(device, call)
     if st != FWT_OK:
         what = (f"fwt_mask_{key}(mask={mask:#x})" if mask is not None else
                 f"fwt_batched_{key}" if bits is None else f"fwt_bits_{key}(bits={tuple(bits)})")

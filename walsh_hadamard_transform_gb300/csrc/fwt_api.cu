@@ -309,6 +309,7 @@ cudaError_t ensure_device() {
 }
 
 std::atomic<int> g_tma_promotion{128};
+std::atomic<int> g_pdl{1};  // launch pass kernels with programmatic stream serialisation
 std::once_flag g_encoder_once;
 PFN_cuTensorMapEncodeTiled_v12000 g_encoder = nullptr;
 
@@ -832,7 +833,55 @@ int run_phase(const float* re_in, const float* im_in, const float* theta, int64_
 }  // namespace
 
 int tma_l2_promotion() { return g_tma_promotion.load(); }
+int pdl_mode() { return g_pdl.load(std::memory_order_relaxed); }
 void set_last_cuda_error(int err) { g_last_cuda_error = err; }
+
+bool tensor_map_2d(CUtensorMap* out, CUtensorMapDataType dt, void* base, const cuuint64_t dims[2],
+                   cuuint64_t row_stride_bytes, const cuuint32_t box[2], int l2_promotion) {
+  struct Entry {
+    bool valid;
+    CUtensorMapDataType dt;
+    void* base;
+    cuuint64_t dims[2], stride;
+    cuuint32_t box[2];
+    int promo;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 8;
+  thread_local Entry cache[kEntries] = {};
+  thread_local int next = 0;
+  for (Entry& e : cache)
+    if (e.valid && e.dt == dt && e.base == base && e.dims[0] == dims[0] && e.dims[1] == dims[1] &&
+        e.stride == row_stride_bytes && e.box[0] == box[0] && e.box[1] == box[1] &&
+        e.promo == l2_promotion) {
+      *out = e.map;
+      return true;
+    }
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const CUtensorMapL2promotion prom = l2_promotion == 256   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                                      : l2_promotion == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                      : l2_promotion == 64  ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B
+                                                            : CU_TENSOR_MAP_L2_PROMOTION_NONE;
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(out, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_NONE, prom, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Entry& e = cache[next];
+  next = (next + 1) % kEntries;
+  e.valid = true;
+  e.dt = dt;
+  e.base = base;
+  e.dims[0] = dims[0];
+  e.dims[1] = dims[1];
+  e.stride = row_stride_bytes;
+  e.box[0] = box[0];
+  e.box[1] = box[1];
+  e.promo = l2_promotion;
+  e.map = *out;
+  return true;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   std::call_once(g_encoder_once, [] {
@@ -1033,6 +1082,14 @@ int fwt_set_tma_l2_promotion(int bytes) {
   fwt::g_tma_promotion.store(bytes);
   return FWT_OK;
 }
+
+int fwt_set_pdl(int mode) {
+  if (mode < 0 || mode > 1) return FWT_ERR_INVALID_ARG;
+  fwt::g_pdl.store(mode);
+  return FWT_OK;
+}
+
+int fwt_get_pdl(void) { return fwt::g_pdl.load(); }
 
 int fwt_get_tma(void) {
   std::lock_guard<std::mutex> lk(fwt::g_plan_mu);

@@ -619,6 +619,7 @@ __device__ __forceinline__ void tile_body(const PassParams& p, unsigned char* sm
 
 template <class S, int KIND, bool COLS>
 __global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1)) fwt_tile_kernel(const PassParams p) {
+  pdl_begin();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   DirectMover<S, COLS> mv(p, smem_raw);
   tile_body<S, KIND>(p, smem_raw, mv, StaticBits<S>(p));
@@ -630,6 +631,7 @@ template <class S, int KIND>
 __global__ void __launch_bounds__(S::NT, KIND == 1 ? (S::NT < 768 ? 768 / S::NT : 1)
                                                    : (S::NT < 512 ? 512 / S::NT : 1))
     fwt_row_bulk_kernel(const PassParams p) {
+  pdl_begin();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bar;
   BulkMover<S> mv(p, smem_raw, &bar);
@@ -641,6 +643,7 @@ template <class S, int KIND>
 __global__ void __launch_bounds__(S::NT, KIND == 1 ? (S::NT < 768 ? 768 / S::NT : 1)
                                                    : (S::NT < 512 ? 512 / S::NT : 1))
     fwt_rowbits_bulk_kernel(const PassParams p) {
+  pdl_begin();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bar;
   BulkMover<S> mv(p, smem_raw, &bar);
@@ -653,6 +656,7 @@ __global__ void __launch_bounds__(S::NT, KIND == 1 ? (S::NT < 768 ? 768 / S::NT 
 template <class S, int KIND>
 __global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
     fwt_rowbits_kernel(const PassParams p) {
+  pdl_begin();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   DirectMover<S, false, true> mv(p, smem_raw);
   tile_body<S, KIND>(p, smem_raw, mv, RuntimeBits<S>(p));
@@ -672,6 +676,7 @@ constexpr int col_tma_min_blocks(int kind) {
 template <class S, int KIND>
 __global__ void __launch_bounds__(S::NT, col_tma_min_blocks<S>(KIND))
     fwt_col_tma_kernel(const __grid_constant__ TmaPassParams tp) {
+  pdl_begin();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ __align__(8) uint64_t bar;
   TmaMover<S, (KIND == 1 || KIND == 3) ? 8 : 4> mv(tp, smem_raw, &bar);
@@ -978,6 +983,7 @@ __device__ __forceinline__ void cluster_plain_body(const PassParams& p, unsigned
 template <class S, int KIND, int CL>
 __global__ void __launch_bounds__(S::NT, (S::NT < 768 ? 768 / S::NT : 1))
     fwt_cluster_kernel(const PassParams p) {
+  pdl_begin();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   if constexpr (KIND == 1) {
     __shared__ __align__(8) uint64_t bar;
@@ -995,6 +1001,7 @@ __global__ void __launch_bounds__(S::NT, (S::NT < 768 ? 768 / S::NT : 1))
 template <class S>
 __global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
     fwt_phase_row_kernel(const PassParams p) {
+  pdl_begin();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   float* sm = reinterpret_cast<float*>(smem_raw);
   const auto m = TileMap<S, false, true>::make(p, (long long)blockIdx.x);
@@ -1042,6 +1049,7 @@ __global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
 // The same for vectors of 2^NL <= 4 elements: one thread per vector.
 template <int NL>
 __global__ void __launch_bounds__(256) fwt_phase_small_kernel(const PassParams p) {
+  pdl_begin();
   const long long row = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (row >= (p.comp_elems >> NL)) return;
   const float* in_re = static_cast<const float*>(p.in[0]);
@@ -1068,6 +1076,7 @@ __global__ void __launch_bounds__(256) fwt_phase_small_kernel(const PassParams p
 // Vectors of 2^NL <= 4 elements: one thread per vector, plain arithmetic.
 template <typename T, class A, int NL>
 __global__ void __launch_bounds__(256) fwt_small_kernel(const PassParams p) {
+  pdl_begin();
   const bool im = blockIdx.y != 0;
   const T* in = static_cast<const T*>(im ? p.in[1] : p.in[0]);
   T* out = static_cast<T*>(im ? p.out[1] : p.out[0]);

@@ -44,6 +44,39 @@ __host__ __device__ constexpr int choose_el(int TB, int LV) {
   return (TB - 5 + LV + 1) / 2 > 5 ? (TB - 5 + LV + 1) / 2 : 5;
 }
 
+// Whether pass kernels are launched with programmatic stream serialisation (see
+// pdl_begin in tma.cuh); set with fwt_set_pdl.
+int pdl_mode();
+
+// Launches a pass kernel: `cluster` > 1 groups its CTAs into thread-block clusters,
+// and with PDL on it may start while the previous kernel on the stream drains.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pass(void (*kernel)(KArgs...), dim3 grid, unsigned threads, size_t smem,
+                        cudaStream_t st, unsigned cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl_mode()) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ---- host-side checks of a tile shape ----------------------------------------------
 template <class S>
 uint32_t host_idx(int layout, uint32_t t, uint32_t r) {
@@ -199,12 +232,10 @@ cudaError_t launch_tile(const PassParams& p, long long tiles, int ncomp, cudaStr
   const dim3 grid((unsigned)tiles, (unsigned)ncomp);
   if constexpr (has_bulk_row<S, KIND, COLS>()) {
     if (p.bulk && (p.comp_elems & ((1ll << S::TB) - 1)) == 0) {
-      fwt_row_bulk_kernel<S, KIND><<<grid, S::NT, smem, st>>>(p);
-      return cudaGetLastError();
+      return launch_pass(fwt_row_bulk_kernel<S, KIND>, grid, S::NT, smem, st, 1, p);
     }
   }
-  fwt_tile_kernel<S, KIND, COLS><<<grid, S::NT, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pass(fwt_tile_kernel<S, KIND, COLS>, grid, S::NT, smem, st, 1, p);
 }
 template <class S, int KIND, bool COLS>
 cudaError_t setup_tile() {
@@ -220,13 +251,19 @@ cudaError_t setup_tile() {
 
 template <typename T, class A, int NL>
 cudaError_t launch_small(const PassParams& p, long long tiles, int ncomp, cudaStream_t st) {
-  fwt_small_kernel<T, A, NL><<<dim3((unsigned)tiles, (unsigned)ncomp), 256, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pass(fwt_small_kernel<T, A, NL>, dim3((unsigned)tiles, (unsigned)ncomp), 256, 0, st,
+                     1, p);
 }
 inline int selfcheck_none() { return 0; }
 
 // The driver's tensor-map encoder, resolved once at run time (nullptr if absent).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+// A 2-D tiled tensor map (no interleave, no swizzle, no fill), from a small
+// per-thread cache of recently encoded maps: a transform called again on the same
+// buffers reuses them instead of encoding again.  false if the encoder is missing
+// or refuses the arguments.
+bool tensor_map_2d(CUtensorMap* out, CUtensorMapDataType dt, void* base, const cuuint64_t dims[2],
+                   cuuint64_t row_stride_bytes, const cuuint32_t box[2], int l2_promotion);
 // L2 sector promotion of TMA column tiles, in bytes (0, 64, 128 or 256).
 int tma_l2_promotion();
 
@@ -243,25 +280,18 @@ cudaError_t launch_col_tma(const PassParams& p, long long tiles, int ncomp, cuda
   const cuuint64_t dims[2] = {1ull << p.stride_log, rows};
   const cuuint64_t strides[1] = {(cuuint64_t)esz << p.stride_log};
   const cuuint32_t box[2] = {1u << S::TS, (cuuint32_t)TmaMover<S, (KIND == 1 || KIND == 3) ? 8 : 4>::BOXR};
-  const cuuint32_t estr[2] = {1, 1};
   TmaPassParams tp;
   tp.p = p;
+  const int promo = tma_l2_promotion();
   for (int c = 0; c < ncomp; ++c) {
     if (p.in[c] != p.out[c]) return cudaErrorInvalidValue;  // column passes run in place
-    const int promo = tma_l2_promotion();
-    const CUtensorMapL2promotion prom = promo == 256   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
-                                        : promo == 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
-                                        : promo == 64  ? CU_TENSOR_MAP_L2_PROMOTION_L2_64B
-                                                       : CU_TENSOR_MAP_L2_PROMOTION_NONE;
-    const CUresult r = enc(&tp.map[c], dt, 2, p.out[c], dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, prom,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    if (!tensor_map_2d(&tp.map[c], dt, p.out[c], dims, strides[0], box, promo))
+      return cudaErrorInvalidValue;
   }
   if (ncomp == 1) tp.map[1] = tp.map[0];
   const size_t smem = (size_t)esz << S::TB;
-  fwt_col_tma_kernel<S, KIND><<<dim3((unsigned)tiles, (unsigned)ncomp), S::NT, smem, st>>>(tp);
-  return cudaGetLastError();
+  return launch_pass(fwt_col_tma_kernel<S, KIND>, dim3((unsigned)tiles, (unsigned)ncomp), S::NT, smem,
+                     st, 1, tp);
 }
 template <class S, int KIND>
 cudaError_t setup_col_tma() {
@@ -322,12 +352,10 @@ cudaError_t launch_rowbits(const PassParams& p, long long tiles, int ncomp, cuda
   const dim3 grid((unsigned)tiles, (unsigned)ncomp);
   if constexpr (has_bulk_row<S, KIND, false>()) {
     if (p.bulk && (p.comp_elems & ((1ll << S::TB) - 1)) == 0) {
-      fwt_rowbits_bulk_kernel<S, KIND><<<grid, S::NT, smem, st>>>(p);
-      return cudaGetLastError();
+      return launch_pass(fwt_rowbits_bulk_kernel<S, KIND>, grid, S::NT, smem, st, 1, p);
     }
   }
-  fwt_rowbits_kernel<S, KIND><<<grid, S::NT, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pass(fwt_rowbits_kernel<S, KIND>, grid, S::NT, smem, st, 1, p);
 }
 template <class S, int KIND>
 cudaError_t setup_rowbits() {
@@ -382,8 +410,7 @@ KernelEntry rowbits_entry() {
 template <class S>
 cudaError_t launch_phase_row(const PassParams& p, long long tiles, int, cudaStream_t st) {
   const size_t smem = (size_t)4 << S::TB;
-  fwt_phase_row_kernel<S><<<(unsigned)tiles, S::NT, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pass(fwt_phase_row_kernel<S>, dim3((unsigned)tiles), S::NT, smem, st, 1, p);
 }
 template <class S>
 cudaError_t setup_phase_row() {
@@ -392,8 +419,7 @@ cudaError_t setup_phase_row() {
 }
 template <int NL>
 cudaError_t launch_phase_small(const PassParams& p, long long tiles, int, cudaStream_t st) {
-  fwt_phase_small_kernel<NL><<<(unsigned)tiles, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pass(fwt_phase_small_kernel<NL>, dim3((unsigned)tiles), 256, 0, st, 1, p);
 }
 
 // fp32 phase-then-transform first pass over bits [0, K) (K <= 2: a thread per vector).
@@ -422,19 +448,8 @@ KernelEntry phase_entry() {
 
 template <class S, int KIND, int CL>
 cudaError_t launch_cluster(const PassParams& p, long long tiles, int ncomp, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)tiles, (unsigned)ncomp, 1);
-  cfg.blockDim = dim3(S::NT, 1, 1);
-  cfg.dynamicSmemBytes = (size_t)(KIND == 1 ? 8 : 4) << S::TB;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1u << CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fwt_cluster_kernel<S, KIND, CL>, p);
+  return launch_pass(fwt_cluster_kernel<S, KIND, CL>, dim3((unsigned)tiles, (unsigned)ncomp),
+                     S::NT, (size_t)(KIND == 1 ? 8 : 4) << S::TB, st, 1u << CL, p);
 }
 template <class S, int KIND, int CL>
 cudaError_t setup_cluster() {

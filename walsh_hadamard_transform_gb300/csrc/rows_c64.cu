@@ -13,6 +13,7 @@ __global__ void __launch_bounds__(256) fwt_phase_apply_c64_kernel(
     const double* re_in, const double* im_in, const double* theta, long long theta_stride,
     double* re_out, double* im_out,
     int n, long long pairs) {
+  pdl_begin();
   const long long nmask = (1ll << n) - 1;
   for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < pairs;
        q += (long long)gridDim.x * blockDim.x) {
@@ -33,6 +34,7 @@ __global__ void __launch_bounds__(256) fwt_phase_apply_c64_kernel(
 __global__ void __launch_bounds__(256) fwt_phase_apply_c64_scalar_kernel(
     const double* re_in, const double* im_in, const double* theta, long long theta_stride,
     double* re_out, double* im_out, long long count) {
+  pdl_begin();
   for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < count;
        e += (long long)gridDim.x * blockDim.x) {
     double s, c;
@@ -51,12 +53,10 @@ cudaError_t launch_phase_apply_c64(const double* re_in, const double* im_in, con
   const long long want = (work + 255) / 256;
   const unsigned blocks = (unsigned)std::max<long long>(1, std::min<long long>(want, (long long)sms * 8));
   if (n >= 1)
-    fwt_phase_apply_c64_kernel<<<blocks, 256, 0, st>>>(re_in, im_in, theta, theta_stride, re_out,
-                                                       im_out, n, work);
-  else
-    fwt_phase_apply_c64_scalar_kernel<<<blocks, 256, 0, st>>>(re_in, im_in, theta, theta_stride,
-                                                              re_out, im_out, work);
-  return cudaGetLastError();
+    return launch_pass(fwt_phase_apply_c64_kernel, dim3(blocks), 256, 0, st, 1, re_in, im_in, theta,
+                       theta_stride, re_out, im_out, n, work);
+  return launch_pass(fwt_phase_apply_c64_scalar_kernel, dim3(blocks), 256, 0, st, 1, re_in, im_in,
+                     theta, theta_stride, re_out, im_out, work);
 }
 
 void register_rows_c64(std::vector<KernelEntry>& v) {

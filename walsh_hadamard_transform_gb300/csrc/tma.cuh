@@ -23,6 +23,17 @@ namespace fwt {
 static __device__ unsigned int g_device_error;
 constexpr unsigned int kErrTmaTimeout = 1u;
 
+// Programmatic dependent launch: the pass kernels are launched so that they may
+// start while the previous kernel on their stream is still draining.  Each waits
+// here, before its first global-memory access, until that kernel has completed and
+// its writes are visible, and then lets the next kernel on the stream be scheduled
+// (it starts once every CTA of this grid has started, so nothing of this grid can
+// be left unscheduled behind it).  Without the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
