@@ -152,14 +152,16 @@ int fwt_phase_c32(const float* re_in, const float* im_in, const float* theta,
 
 /*
  * The same for complex fp64 with fp64 angles: theta is a DEVICE array of doubles,
- * 16-byte aligned, theta_stride even when n >= 1.  The phase comes from the
- * double-precision sincos, applied element by element into the outputs, and the
- * fp64 transform then runs in place on them (one extra read and write of the data:
- * fusing the phase into the fixed-point row pass would make the CTAs of both parts
- * evaluate every sine and cosine on the fp64 unit, which costs more).  The relative
- * L2 error per vector stays below 1e-12 of the exact result for angles of moderate
- * size (|theta| up to about 1e3; the phase error grows with |theta| as the sincos
- * argument's own rounding does).  Other arguments and errors as fwt_phase_c32.
+ * 16-byte aligned, theta_stride even when n >= 1.  The phase is applied element by
+ * element into the outputs, and the fp64 transform then runs in place on them.  The
+ * sine and cosine are evaluated in 64-bit integer arithmetic (GB300's fp64 unit is
+ * slow): the angle reduced to a 64-bit fraction of a turn with 1/(2 pi) held to 128
+ * bits, a 1024-entry table of cos/sin and short Taylor series for the remainder,
+ * the rotation in fixed point with one rounding back to fp64; each rotated element
+ * is within about 1e-16 of the exact rotation of its angle, relative to its
+ * magnitude, for |theta| < 2^40.  Elements with an Inf or NaN, and angles of 2^40
+ * and more, use the double-precision sincos instead.  Other arguments and errors as
+ * fwt_phase_c32.
  */
 int fwt_phase_c64(const double* re_in, const double* im_in, const double* theta,
                   int64_t theta_stride, double* re_out, double* im_out, int n, int64_t batch,

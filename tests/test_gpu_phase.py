@@ -101,3 +101,69 @@ def test_phase_fp64_n24_and_errors():
     assert fwt.fwt_phase_c64(*p, t.data_ptr(), 3, *o, 6, 1, 1, None) == fwt.FWT_ERR_MISALIGNED
     assert fwt.fwt_phase_c64(*p, y.data_ptr(), 0, *o, 6, 1, 1, None) == fwt.FWT_ERR_INVALID_ARG
     torch.cuda.synchronize()
+
+
+def test_phase_fp64_angles_to_1e3_match_oracle():
+    """fp64 phase with angles of up to 1e3 rad (fixed-point sine and cosine), then the
+    transform: within the fp64 specification of the oracle (libm sin/cos, double)."""
+    rng = np.random.default_rng(7)
+    for n, batch in ((12, 3), (16, 2), (24, 1)):
+        re, im = inputs.random_pair(n, batch, "c64", seed=80 + n)
+        th = rng.uniform(-1e3, 1e3, size=(batch, 1 << n))
+        ore, oim = oracle.phase_fwt(re, im, th, normalize=True)
+        gre, gim = _run(re, im, th, True)
+        err = rel_err_per_vector(gre, gim, ore, oim)
+        assert err.max() <= TOL["c64"], f"n={n}: {err.max():.3e}"
+
+
+def _angles(rng, size):
+    parts = [rng.uniform(-1e3, 1e3, size), rng.uniform(-np.pi, np.pi, size),
+             np.round(rng.uniform(-600, 600, size)) * (np.pi / 2) + rng.uniform(-1e-9, 1e-9, size),
+             rng.uniform(-1e-6, 1e-6, size), rng.uniform(-1e12, 1e12, size),
+             np.array([0.0, -0.0, 5e-324, -1e-300, 1e-150, np.pi, -np.pi / 2, 2 * np.pi, 1e11,
+                       -1.0995e12])]
+    return np.concatenate(parts)
+
+
+def test_phase_fp64_rotation_matches_cuda_sincos():
+    """n = 0 and x = 1: the phase alone, (cos t, sin t), against CUDA's double-precision
+    cos and sin (torch on the device), for angles across [-1e12, 1e12] including
+    multiples of pi/2, tiny angles and signed zeros; non-finite angles and angles
+    beyond 2^40 rad (the fp64 sincos fallback) give what CUDA's sincos gives."""
+    rng = np.random.default_rng(11)
+    th = _angles(rng, 4000)
+    th = np.concatenate([th, [np.inf, -np.inf, np.nan, 3e12, -1e15, 1e300]])
+    one = np.ones((th.size, 1)); zero = np.zeros_like(one)
+    gre, gim = _run(one, zero, th[:, None], False)
+    t = torch.from_numpy(th).cuda()
+    cre, cim = torch.cos(t).cpu().numpy(), torch.sin(t).cpu().numpy()
+    fin = np.isfinite(cre)
+    assert np.array_equal(np.isnan(gre[:, 0]), np.isnan(cre)) and np.array_equal(np.isnan(gim[:, 0]), np.isnan(cim))
+    assert np.max(np.abs(gre[fin, 0] - cre[fin])) <= 5e-16
+    assert np.max(np.abs(gim[fin, 0] - cim[fin])) <= 5e-16
+
+
+def test_phase_fp64_element_magnitudes():
+    """Elements from subnormal to 1e250 (one exponent per element pair in the fixed
+    point rotation; results near the subnormal range take the exact integer rounding),
+    and Inf/NaN elements (the fp64 fallback), against the oracle."""
+    rng = np.random.default_rng(12)
+    n = 10
+    re, im = inputs.random_pair(n, 4, "c64", seed=90)
+    re[0] *= 1e250; im[0] *= 1e-250
+    re[1] *= 1e-300; im[1] *= 1e-305
+    re[2] = 4e-320 * np.sign(re[2]); im[2] = -7e-321
+    th = rng.uniform(-1e3, 1e3, size=(4, 1 << n))
+    ore, oim = oracle.phase_fwt(re, im, th, normalize=True)
+    gre, gim = _run(re, im, th, True)
+    err = rel_err_per_vector(gre, gim, ore, oim)
+    assert err[:2].max() <= TOL["c64"] and err[3] <= TOL["c64"], err
+    # subnormal elements: the oracle's own double products round on the subnormal grid
+    # (5e-324 apart), so compare absolutely (2^10 terms, each off by a few grid steps)
+    assert max(np.abs(gre[2] - ore[2]).max(), np.abs(gim[2] - oim[2]).max()) <= 1e-319
+    re2, im2 = re.copy(), im.copy()
+    re2[3, 5] = np.inf; im2[3, 7] = np.nan
+    gre, gim = _run(re2, im2, th, False)
+    assert np.isnan(gre[3]).any() and np.isnan(gim[3]).any()
+    ore, oim = oracle.phase_fwt(re2[:2], im2[:2], th[:2], normalize=False)
+    assert rel_err_per_vector(gre[:2], gim[:2], ore, oim).max() <= TOL["c64"]

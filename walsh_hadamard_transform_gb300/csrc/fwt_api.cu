@@ -294,6 +294,8 @@ cudaError_t ensure_device() {
     err = e.setup();
     if (err != cudaSuccess) return err;
   }
+  err = setup_phase_table_c64();
+  if (err != cudaSuccess) return err;
   int l2 = 0;
   err = cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
   if (err != cudaSuccess) return err;
@@ -727,9 +729,16 @@ int run_phase_c64(const double* re_in, const double* im_in, const double* theta,
     return FWT_ERR_INVALID_ARG;
   cudaError_t err = ensure_device();
   const int sms = prefetch_ahead() / 3;  // SMs of the current device
+  const bool traced = g_trace_count + 2 <= g_trace_capacity;
+  if (err == cudaSuccess && traced)
+    err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count], stream);
   if (err == cudaSuccess)
     err = launch_phase_apply_c64(re_in, im_in, theta, theta_stride, re_out, im_out, n, batch, sms,
                                  stream);
+  if (err == cudaSuccess && traced) {
+    err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count + 1], stream);
+    g_trace_count += 2;
+  }
   if (err != cudaSuccess) {
     g_last_cuda_error = (int)err;
     return FWT_ERR_CUDA;

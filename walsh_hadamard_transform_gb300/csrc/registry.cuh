@@ -518,6 +518,8 @@ KernelEntry small_entry() {
 cudaError_t launch_phase_apply_c64(const double* re_in, const double* im_in, const double* theta,
                                    long long theta_stride, double* re_out, double* im_out, int n,
                                    long long batch, int sms, cudaStream_t st);
+// Fills the fp64 phase kernel's table on the current device (once per device).
+cudaError_t setup_phase_table_c64();
 cudaError_t read_device_error_c32(unsigned int* out);
 // Records a failed CUDA call for fwt_last_cuda_error() (calling thread).
 void set_last_cuda_error(int err);
