@@ -279,9 +279,9 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_key: str):
-    """DRAM bytes per launch of `kernel_key` from the committed ncu summary, or None
-    when there is none or the kernel sources changed since it was captured."""
+def ncu_record(kernel_key: str):
+    """The committed ncu DRAM record of `kernel_key` (profiles/ncu_traffic.json), or
+    None when there is none or the kernel sources changed since it was captured."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -291,7 +291,21 @@ def ncu_traffic(kernel_key: str):
     rec = d.get(kernel_key)
     if not rec or rec.get("source_sha") != kernel_source_hash():
         return None
-    return rec.get("dram_bytes_per_launch")
+    return rec
+
+
+def ncu_traffic(kernel_key: str):
+    """DRAM bytes (read + write) of one launch of `kernel_key` at the specified batch."""
+    rec = ncu_record(kernel_key)
+    return None if rec is None else rec.get("dram_bytes_per_launch")
+
+
+def ncu_bytes_per_vector(kernel_key: str):
+    """DRAM bytes (read + write) a launch of `kernel_key` moves per vector: the slope of a
+    fit over two batch sizes when captured that way (the L2's fixed share of dirty
+    lines at the end of a launch drops out), else one capture divided by its batch."""
+    rec = ncu_record(kernel_key)
+    return None if rec is None else rec.get("dram_bytes_per_vector")
 
 
 # ---- our CUDA path ---------------------------------------------------------------
@@ -335,15 +349,17 @@ def run_ours(args):
 
     bits = tuple(int(v) for v in args.bits.split(",")) if args.bits else None
     if args.phase:
-        parts_idx = [i for i, w in enumerate(parts) if w.dtype == "c32"]
+        parts_idx = [i for i, w in enumerate(parts) if w.dtype in ("c32", "c64")]
         if not parts_idx or bits is not None:
-            raise SystemExit("--phase needs an fp32 workload and no --bits")
+            raise SystemExit("--phase needs a floating-point workload and no --bits")
         parts = [parts[i] for i in parts_idx]
         host = [host[i] for i in parts_idx]
         dev_in = [dev_in[i] for i in parts_idx]
         dev_out = [dev_out[i] for i in parts_idx]
         gen = torch.Generator(device=device).manual_seed(rank_seed(11, rank))
-        thetas = [torch.rand(w.batch, w.N, device=device, generator=gen) * (2 * np.pi) for w in parts]
+        thetas = [torch.rand(w.batch, w.N, device=device, generator=gen,
+                             dtype=torch.float64 if w.dtype == "c64" else torch.float32) * (2 * np.pi)
+                  for w in parts]
 
     def step():
         for pi, (w, (a, b), (c, d)) in enumerate(zip(parts, dev_in, dev_out)):
@@ -413,7 +429,7 @@ def run_ours(args):
         mean_ms = statistics.mean(per_kernel[li])
         algo = 2 * parts[pi].bytes_in  # every pass reads and writes the whole batch once
         if args.phase and li == [i for i, o in enumerate(owners) if o == pi][0]:
-            algo += algo // 4  # the first pass also reads the angles (fp32, one per amplitude)
+            algo += algo // 4  # the first pass also reads the angles (one per amplitude)
         kernels.append({"kernel": nm, "mean_ms": mean_ms,
                         "median_ms": statistics.median(per_kernel[li]), "min_ms": min(per_kernel[li]),
                         "total_ms": sum(per_kernel[li]),
@@ -429,10 +445,10 @@ def run_ours(args):
     for pi, w in enumerate(parts):
         ks = [k for k, o in zip(kernels, owners) if o == pi]
         vec = w.bytes_in // w.batch  # re + im of one vector
-        meas = [traffic_of(k["kernel"]) for k in ks]
+        meas = [ncu_bytes_per_vector(k["kernel"]) if args.batch <= 0 else None for k in ks]
         per_vector.append({"part": w.name, "passes": len(ks), "model": 2 * len(ks) * vec,
                            "one_round_trip": 2 * vec,
-                           "measured": (sum(meas) // w.batch
+                           "measured": (int(sum(meas))
                                         if meas and all(m is not None for m in meas) else None)})
     roofline = {"bound": "hbm", "achieved": round(top["gbs"], 1), "peak": peak, "unit": "GB/s",
                 "frac": round(top["gbs"] / peak, 4), "traffic": traffic,
@@ -598,6 +614,10 @@ def measure_config(label, w, fwt, device, peak, reuse=None):
         "eager_us_per_step": round(eager_us, 3),
         "kernels": kernels,
     }
+    meas = [ncu_bytes_per_vector(k["kernel"]) for k in kernels]
+    entry["dram_bytes_per_vector"] = {
+        "model": 2 * npass * (w.bytes_in // w.batch), "one_round_trip": 2 * (w.bytes_in // w.batch),
+        "measured": int(sum(meas)) if all(m is not None for m in meas) else None}
     # the vectors the CPU leg checks against the oracle: all of them up to n = 18, the
     # first and the last at n = 24
     rows = list(range(w.batch)) if w.n <= 18 else [0, w.batch - 1]

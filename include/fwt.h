@@ -342,14 +342,15 @@ int fwt_set_cluster(int mode);
 int fwt_get_cluster(void);
 
 /*
- * Launch overlap: mode 1 (default) launches every pass kernel with programmatic
- * stream serialisation, so it may be scheduled while the previous kernel on the
- * same stream is still finishing; each kernel waits (griddepcontrol.wait) before
- * its first global-memory access until that kernel has completed and its writes
- * are visible, so ordering on the stream is as without it.  It shortens back-to-back
- * launches of small transforms and the gap between the passes of one transform.
- * Mode 0 launches them plainly.  Results are identical.  Returns FWT_OK or
- * FWT_ERR_INVALID_ARG; fwt_get_pdl returns the mode.
+ * Launch overlap: mode 1 (default) launches pass kernels of up to 2048 CTAs with
+ * programmatic stream serialisation, so one may be scheduled while the previous
+ * kernel on the same stream is still finishing; each kernel waits
+ * (griddepcontrol.wait) before its first global-memory access until that kernel has
+ * completed and its writes are visible, so ordering on the stream is as without it.
+ * It shortens back-to-back launches of small transforms (larger grids launch
+ * plainly: there it measured neutral or slower).  Mode 0 launches every kernel
+ * plainly.  Results are identical.  Returns FWT_OK or FWT_ERR_INVALID_ARG;
+ * fwt_get_pdl returns the mode.
  */
 int fwt_set_pdl(int mode);
 int fwt_get_pdl(void);

@@ -49,7 +49,11 @@ __host__ __device__ constexpr int choose_el(int TB, int LV) {
 int pdl_mode();
 
 // Launches a pass kernel: `cluster` > 1 groups its CTAs into thread-block clusters,
-// and with PDL on it may start while the previous kernel on the stream drains.
+// and with PDL on a grid of up to kPdlMaxCtas CTAs may start while the previous kernel
+// on the stream drains.  That shortens back-to-back launch-bound transforms (n = 10 ..
+// 14, batch 64: 5-13% a step); on grids of many waves it measured neutral (fp64,
+// n = 24) or slower (fp32 n = 24: 13%), so those launch plainly.
+constexpr unsigned long long kPdlMaxCtas = 2048;
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pass(void (*kernel)(KArgs...), dim3 grid, unsigned threads, size_t smem,
                         cudaStream_t st, unsigned cluster, Args... args) {
@@ -67,7 +71,7 @@ cudaError_t launch_pass(void (*kernel)(KArgs...), dim3 grid, unsigned threads, s
     attr[na].val.clusterDim.z = 1;
     ++na;
   }
-  if (pdl_mode()) {
+  if (pdl_mode() && (unsigned long long)grid.x * grid.y * grid.z <= kPdlMaxCtas) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
