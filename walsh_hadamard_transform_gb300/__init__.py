@@ -437,24 +437,32 @@ def _dtype_key(t) -> str:
     return key
 
 
+_raw_stream = None
+_get_device = None
+
+
 def _stream_handle(stream, device):
     """The raw cudaStream_t of ``stream`` (default: the current PyTorch stream of
     ``device``)."""
+    global _raw_stream
     if stream is not None:
         return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    torch = _torch_mod()
-    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
-    if raw is not None:
-        return raw(device.index)
-    return torch.cuda.current_stream(device).cuda_stream
+    if _raw_stream is None:
+        torch = _torch_mod()
+        _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None) or (
+            lambda index: torch.cuda.current_stream(index).cuda_stream)
+    return _raw_stream(device.index)
 
 
 def _on_device(device, call):
     """Runs ``call`` with ``device`` current (switching only when it is not)."""
-    torch = _torch_mod()
-    if device.index == torch.cuda.current_device():
+    global _get_device
+    if _get_device is None:
+        torch = _torch_mod()
+        _get_device = getattr(torch._C, "_cuda_getDevice", None) or torch.cuda.current_device
+    if device.index == _get_device():
         return call()
-    with torch.cuda.device(device):
+    with _torch_mod().cuda.device(device):
         return call()
 
 
@@ -470,26 +478,28 @@ def transform(re, im=None, out_re=None, out_im=None, normalize: bool = True, str
     (an int below 2^n) transforms the index bits set in it.  Returns
     (out_re, out_im).
     """
-    torch = _torch_mod()
+    torch = _torch or _torch_mod()
     key = _dtype_key(re)
-    if not re.is_cuda:
+    dtype, shape, device = re.dtype, re.shape, re.device
+    if device.type != "cuda":
         raise ValueError("transform() needs CUDA tensors; use transform_host() for host arrays")
-    if re.dim() != 2:
+    if len(shape) != 2:
         raise ValueError("expected a (batch, 2^n) tensor")
-    batch, N = re.shape
+    batch, N = shape
     n = int(N).bit_length() - 1
     if N < 1 or (1 << n) != N:
         raise ValueError(f"row length {N} is not a power of two")
     if bits is not None and mask is not None:
         raise ValueError("give bits or mask, not both")
+    if not re.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    # outputs made here match re; tensors given by the caller are checked
+    given = [t for t in (im, out_re, out_im) if t is not None]
     if out_re is None:
         out_re = torch.empty_like(re)
     if im is not None and out_im is None:
         out_im = torch.empty_like(im)
-    dtype, shape, device = re.dtype, re.shape, re.device
-    for t in (re, im, out_re, out_im):
-        if t is None:
-            continue
+    for t in given:
         if t.dtype != dtype or t.shape != shape or t.device != device:
             raise ValueError("re, im and outputs must share dtype, shape and device")
         if not t.is_contiguous():
