@@ -188,6 +188,18 @@ def test_bit_range_argument_errors_before_launch(lib, fn):
     assert f(None, None, None, None, 8, 0, 0, 3, 0, None) == fwt.FWT_OK     # empty batch
 
 
+def test_pdl_setting(lib):
+    assert fwt.pdl() == 1
+    fwt.set_pdl(0)
+    assert fwt.pdl() == 0
+    with pytest.raises(fwt.FwtError):
+        fwt.set_pdl(2)
+    with pytest.raises(fwt.FwtError):
+        fwt.set_pdl(-1)
+    fwt.set_pdl(1)
+    assert fwt.pdl() == 1
+
+
 def test_cluster_setting(lib):
     assert fwt.cluster() == fwt.CLUSTER_AUTO
     fwt.set_cluster(fwt.CLUSTER_NEVER)

@@ -43,3 +43,27 @@ def test_peak_falls_back_without_the_measured_file(monkeypatch, tmp_path):
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 1234.5}))
     peak, source = bench.measured_peaks()
     assert peak == 1234.5 and source.startswith("measured")
+
+
+def test_headline_passes_have_fitted_records(monkeypatch):
+    """The four n = 24 passes carry a batch-2/4 fit; bench.py reports its per-vector
+    bytes and the fit at batch 16, only while the sources are those it was captured from."""
+    path = os.path.join(bench.ROOT, "profiles", "ncu_traffic.json")
+    records = json.load(open(path))
+    keys = ["c64 row pass K=13 (n=24)", "c64 col pass K=11 (n=24)",
+            "c32 row pass K=14 (n=24)", "c32 col pass K=10 (n=24)"]
+    for key in keys:
+        rec = records[key]
+        fit = rec["batch_fit"]
+        per = fit["read_per_vector"] + fit["write_per_vector"]
+        assert rec["dram_bytes_per_vector"] == per
+        at16 = fit["read_intercept"] + fit["write_intercept"] + 16 * per
+        assert abs(rec["dram_bytes_per_launch"] - at16) <= 16
+        # both captures lie on the fitted line
+        for b, r, w in zip(fit["batches"], fit["read_bytes"], fit["write_bytes"]):
+            assert abs(r - (fit["read_intercept"] + b * fit["read_per_vector"])) <= 4
+            assert abs(w - (fit["write_intercept"] + b * fit["write_per_vector"])) <= 4
+        monkeypatch.setattr(bench, "kernel_source_hash", lambda: rec["source_sha"])
+        assert bench.ncu_bytes_per_vector(key) == per
+        monkeypatch.setattr(bench, "kernel_source_hash", lambda: "f" * 16)
+        assert bench.ncu_bytes_per_vector(key) is None

@@ -266,14 +266,19 @@ std::vector<long long> g_dev_l2;  // L2 bytes per device
 std::vector<int> g_dev_sms;       // SMs per device
 long long g_chunk_bytes = 0;       // -1: half the L2 of the current device; 0: off (default)
 
-// Tiles one wave of the three-CTA-an-SM staged kernels covers: how far ahead their
-// L2 prefetch reaches (the tile that starts on a CTA slot when the current one ends).
-int prefetch_ahead() {
+// SMs of the current device (0 before its set-up).
+int device_sms() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   std::lock_guard<std::mutex> lk(g_dev_mu);
-  return dev < (int)g_dev_sms.size() ? 3 * g_dev_sms[dev] : 0;
+  return dev < (int)g_dev_sms.size() ? g_dev_sms[dev] : 0;
 }
+
+// How far ahead (in tiles) the staged kernels' L2 prefetch reaches: two tiles an SM,
+// two thirds of a wave of the three-CTA-an-SM kernels (measured against one and
+// more waves ahead: the fp64 n = 24 row pass 1.551 ms at two tiles an SM, 1.575 at
+// three, 1.609 at four, 1.781 at six, 1.611 without prefetch).
+int prefetch_ahead() { return 2 * device_sms(); }
 
 long long chunk_budget() {
   int dev = 0;
@@ -728,7 +733,7 @@ int run_phase_c64(const double* re_in, const double* im_in, const double* theta,
   if (overlaps2(theta, th_bytes, re_out, bytes) || overlaps2(theta, th_bytes, im_out, bytes))
     return FWT_ERR_INVALID_ARG;
   cudaError_t err = ensure_device();
-  const int sms = prefetch_ahead() / 3;  // SMs of the current device
+  const int sms = device_sms();
   const bool traced = g_trace_count + 2 <= g_trace_capacity;
   if (err == cudaSuccess && traced)
     err = cudaEventRecord((cudaEvent_t)g_trace_events[g_trace_count], stream);
