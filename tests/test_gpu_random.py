@@ -58,7 +58,10 @@ def _run(c, rng):
     if c["kind"] == "chunk":
         fwt.set_l2_chunk_bytes(int(rng.choice([-1, 1 << 20, 8 << 20, 64 << 20])))
     if c["kind"] == "phase":
-        theta = rng.uniform(-np.pi, np.pi, size=(int(rng.choice([1, batch])), 1 << n)).astype(re.dtype)
+        # fp64 angles at several scales: the fixed-point reduction (up to 2^40 rad) and the
+        # fp64 sincos beyond it
+        span = np.pi if re.dtype == np.float32 else float(rng.choice([np.pi, 1e3, 1e9, 1e13]))
+        theta = rng.uniform(-span, span, size=(int(rng.choice([1, batch])), 1 << n)).astype(re.dtype)
         ore, oim = oracle.phase_fwt(re, im, theta, normalize=norm)
         a, b, t = (torch.from_numpy(v).cuda() for v in (re, im, theta))
         out = (fwt.phase_transform(a, b, t, a, b, normalize=norm) if inplace
