@@ -998,9 +998,12 @@ __global__ void __launch_bounds__(S::NT, (S::NT < 768 ? 768 / S::NT : 1))
 // The first pass of y = s * H (e^{i theta} . x): each CTA loads the real part,
 // the imaginary part and the angles of one row tile, rotates every amplitude by
 // its phase (sincosf), and transforms both rotated parts in turn through the same
-// shared buffer.  Later passes (if any) are ordinary column passes.
+// shared buffer.  Later passes (if any) are ordinary column passes.  Three CTAs an SM
+// (80 registers, a few spilled): the loads of three arrays need the warps more than the
+// registers (at two CTAs an SM, 108 registers, it measured 1.30 ms against 1.09 ms for
+// n = 24, batch 16).
 template <class S>
-__global__ void __launch_bounds__(S::NT, (S::NT < 512 ? 512 / S::NT : 1))
+__global__ void __launch_bounds__(S::NT, (S::NT < 768 ? 768 / S::NT : 1))
     fwt_phase_row_kernel(const PassParams p) {
   pdl_begin();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
