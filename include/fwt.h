@@ -36,7 +36,10 @@
  * synchronisation with `stream`.
  *
  * Thread safety: calls may be made from several host threads and devices; the
- * per-device set-up (kernel attributes) is done once under a lock.
+ * per-device set-up (kernel attributes, and the table of the fp64 phase copied to
+ * the device) is done once under a lock, by the first call on each device: make that
+ * call before capturing transforms into a CUDA graph.  Afterwards the entry points
+ * enqueue only stream work.
  */
 #ifndef FWT_GB300_H
 #define FWT_GB300_H
