@@ -67,3 +67,40 @@ def test_headline_passes_have_fitted_records(monkeypatch):
         assert bench.ncu_bytes_per_vector(key) == per
         monkeypatch.setattr(bench, "kernel_source_hash", lambda: "f" * 16)
         assert bench.ncu_bytes_per_vector(key) is None
+
+
+def test_cpu_leg_checks_gpu_results_against_the_oracle(monkeypatch):
+    """The CPU leg's per-configuration check: exact results report ~0 error (float) or
+    bit-exact (int32); a planted error of known size is reported at that size, and a
+    changed int32 element is not bit-exact."""
+    import dataclasses
+
+    import numpy as np
+
+    import oracle
+    from walsh_hadamard_transform_gb300 import inputs
+
+    monkeypatch.setattr(bench, "cpu_baseline", lambda parts, host, sample: {"value": 0.0})
+    w32 = dataclasses.replace(inputs.WORKLOADS["n10_b64_c32"], batch=4)
+    re, im = w32.generate()
+    ore, oim = oracle.fwt_complex(re, im, normalize=True)
+    bad_re = ore.copy()
+    bad_re[2, 5] += 1e-4 * np.linalg.norm(np.concatenate([ore[2], oim[2]]))  # one element off
+    wi = inputs.Workload("i8", 8, 3, "i32", 5, False, "uniform_int8")
+    ire, iim = wi.generate()
+    iore, ioim = oracle.fwt_complex(ire, iim, normalize=False)
+    ibad = iore.copy()
+    ibad[1, 7] += 1
+    checks = [
+        {"label": "good", "workload": w32, "rows": [0, 1, 2, 3], "host_in": (re, im),
+         "got": (ore.astype(np.float32), oim.astype(np.float32))},
+        {"label": "bad", "workload": w32, "rows": [0, 1, 2, 3], "host_in": (re, im), "got": (bad_re, oim)},
+        {"label": "igood", "workload": wi, "rows": [0, 1, 2], "host_in": (ire, iim), "got": (iore, ioim)},
+        {"label": "ibad", "workload": wi, "rows": [0, 1, 2], "host_in": (ire, iim), "got": (ibad, ioim)},
+    ]
+    _, errors = bench.cpu_leg([], [], 1, checks)
+    assert errors["good"]["max_rel_l2_err"] < 1e-7
+    assert 0.9e-4 < errors["bad"]["max_rel_l2_err"] < 1.1e-4
+    assert errors["igood"]["bit_exact"] is True
+    assert errors["ibad"]["bit_exact"] is False
+    assert errors["good"]["oracle_check"] == "all 4 vectors"
