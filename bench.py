@@ -652,28 +652,39 @@ def run_e2e(args, parts, host, device, fwt, world):
             fwt.transform_host(a, b, ha, hb, normalize=w.normalize, workspace=ws, stream=s,
                                synchronize=False)
 
-    step()
+    main = torch.cuda.current_stream(device)
+    # at least as many untimed steps as the main timed region (the first transfers of freshly
+    # pinned buffers are several times slower than later ones)
+    for _ in range(max(3, args.warmup)):
+        step()
     torch.cuda.synchronize(device)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    ends = [[torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps)] for _ in streams]
     barrier(device)
-    main = torch.cuda.current_stream(device)
     t0.record(main)
     for s in streams:
         s.wait_event(t0)
-    for _ in range(args.e2e_steps):
+    for i in range(args.e2e_steps):
         step()
+        for p, s in enumerate(streams):
+            ends[p][i].record(s)
     for s in streams:
         main.wait_stream(s)
     t1.record(main)
     torch.cuda.synchronize(device)
     barrier(device)
     ms = dist_max(t0.elapsed_time(t1), device)
+    # a step's time: the later of the parts, each from its previous step's end
+    per_step = [max((ends[p][i - 1] if i else t0).elapsed_time(ends[p][i]) for p in range(len(streams)))
+                for i in range(args.e2e_steps)]
     vectors = sum(w.batch for w in parts) * world * args.e2e_steps
     return {"value": round(vectors / (ms / 1e3), 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": h2d, "steps": args.e2e_steps,
-            "ms_per_step": round(ms / args.e2e_steps, 3), "workspace_bytes": sum(ws_each),
-            "streams": len(streams)}
+            "d2h_bytes_per_step": h2d, "steps": args.e2e_steps, "warmup": max(3, args.warmup),
+            "ms_per_step": round(ms / args.e2e_steps, 3),
+            "step_ms": {"median": round(statistics.median(per_step), 3), "min": round(min(per_step), 3),
+                        "max": round(max(per_step), 3)},
+            "workspace_bytes": sum(ws_each), "streams": len(streams)}
 
 
 def oracle_step(orc, parts, host, threads):
