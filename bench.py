@@ -60,7 +60,7 @@ def parse_args(argv=None):
                     help="time the fused phase + transform (fp32 parts; random per-vector angles)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch of every part (small cases for profiling; 0 = as specified)")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=25)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=8,
