@@ -520,6 +520,40 @@ CONFIGS = [("c1", "n10_b64_c32"), ("c2", "n12_b64_c32"), ("c3", "n14_b64_c32"),
            ("c4", "n18_b256_i32"), ("c5a", "n24_b16_c64"), ("c5b", "n24_b16_c32")]
 
 
+def copy_floor_s(nbytes, reps, replays, device):
+    """Seconds per step of the simplest kernel that reads and writes `nbytes` once (one
+    launch of torch's elementwise negation, src -> dst), back to back from a CUDA graph
+    over `reps` buffer pairs: the timing harness of measure_config applied to a plain
+    one-launch streaming step.  (A captured copy_ becomes a graph memcpy node, which
+    measured at half the kernel's rate for large buffers, so it is not used.)"""
+    import torch
+
+    n = nbytes // 4
+    src = [torch.ones(n, dtype=torch.float32, device=device) for _ in range(reps)]
+    dst = [torch.empty_like(src[0]) for _ in range(reps)]
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        for r in range(reps):
+            torch.neg(src[r], out=dst[r])
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for r in range(reps):
+            torch.neg(src[r], out=dst[r])
+    graph.replay()
+    torch.cuda.synchronize(device)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record()
+    for _ in range(replays):
+        graph.replay()
+    g1.record()
+    torch.cuda.synchronize(device)
+    t = g0.elapsed_time(g1) / 1e3 / (replays * reps)
+    del graph, src, dst
+    return t
+
+
 def measure_config(label, w, fwt, device, peak, reuse=None):
     """Throughput of one specified configuration on its own, inputs in HBM.
 
@@ -602,6 +636,7 @@ def measure_config(label, w, fwt, device, peak, reuse=None):
     steps = replays * reps
     step_s = g0.elapsed_time(g1) / 1e3 / steps
     gbs = algo / step_s / 1e9
+    copy_s = copy_floor_s(w.bytes_in, reps, replays, device)
     entry = {
         "config": label, "workload": w.name, "n": w.n, "batch": w.batch, "dtype": w.dtype,
         "normalize": w.normalize, "factors": fwt.plan_factors(w.n, w.dtype), "passes": npass,
@@ -612,6 +647,10 @@ def measure_config(label, w, fwt, device, peak, reuse=None):
                    "inputs read from HBM), replayed %d times" % (reps, reps, reps * set_bytes / 2 ** 20, replays)
                    if small else "CUDA graph of one transform, replayed %d times (inputs larger than L2)" % replays),
         "eager_us_per_step": round(eager_us, 3),
+        # the same bytes read and written once by a plain streaming kernel (torch.neg, one
+        # launch a step, same graph harness): the floor of a one-launch step of this size
+        "copy_floor_us_per_step": round(copy_s * 1e6, 3),
+        "speed_vs_copy": round(copy_s / step_s, 3),
         "kernels": kernels,
     }
     meas = [ncu_bytes_per_vector(k["kernel"]) for k in kernels]
