@@ -96,3 +96,25 @@ def test_host_rejects_device_tensors_and_bad_shapes():
         fwt.transform_host(torch.zeros(2, 8, device="cuda"), torch.zeros(2, 8, device="cuda"))
     with pytest.raises(ValueError):
         fwt.transform_host(torch.zeros(2, 6), torch.zeros(2, 6))
+
+
+@pytest.mark.parametrize("name", ["n24_b16_c64", "n24_b16_c32"])
+def test_host_benchmark_workload(name):
+    """The end-to-end call the benchmark times (n = 24, batch 16, pinned host arrays, the
+    full-depth workspace): the first and last vectors against the oracle, and every
+    vector's norm against Parseval (the normalised transform is orthogonal)."""
+    w = inputs.WORKLOADS[name]
+    re, im = w.generate()
+    a, b = _host_pair(re, im, pinned=True)
+    ws = torch.empty(fwt.fwt_host_workspace_bytes(fwt.DTYPES[w.dtype], w.n, w.batch, True),
+                     dtype=torch.uint8, device="cuda")
+    gre, gim = fwt.transform_host(a, b, normalize=True, workspace=ws)
+    gre, gim = gre.numpy(), gim.numpy()
+    rows = [0, w.batch - 1]
+    ore, oim = oracle.fwt_complex(re[rows], im[rows], normalize=True, nthreads=host_threads())
+    assert_matches(w.dtype, gre[rows], gim[rows], ore, oim, f"host {name} vectors {rows}")
+    tol = 1e-5 if w.dtype == "c32" else 1e-11
+    for v in range(w.batch):
+        n_in = np.sum(re[v].astype(np.float64) ** 2 + im[v].astype(np.float64) ** 2)
+        n_out = np.sum(gre[v].astype(np.float64) ** 2 + gim[v].astype(np.float64) ** 2)
+        assert abs(n_out - n_in) <= tol * n_in, (name, v, n_in, n_out)
