@@ -684,7 +684,7 @@ int run(int dtype, const void* re_in, const void* im_in, void* re_out, void* im_
         p.bits_mask = ps.mask;
         const bool last = f == npass - 1;
         p.do_scale = (normalize && last) ? 1 : 0;
-        p.ld_policy = 1;                             // read once
+        p.ld_policy = 0;                             // normal (evict-first measured slower)
         p.st_policy = last ? 1 : (chunked ? 2 : 0);  // keep intermediates for the next pass
         p.bulk = plan.tma != 0 ? 1 : 0;              // bulk-copied fp64 row tiles
         p.prefetch_ahead = ahead;
@@ -822,7 +822,7 @@ int run_phase(const float* re_in, const float* im_in, const float* theta, int64_
     p.stride_log = passes[f].L;
     const bool last = f == npass - 1;
     p.do_scale = (normalize && last) ? 1 : 0;
-    p.ld_policy = 1;
+    p.ld_policy = 0;
     p.st_policy = last ? 1 : 0;
     const bool traced = g_trace_count + 2 <= g_trace_capacity;
     if (traced) {

@@ -95,10 +95,11 @@ using ArithU32 = ArithInt<uint32_t, uint32_t, false>;  // two's complement wrap,
 using ArithI64 = ArithInt<long long, unsigned long long, true>;
 
 // ---- global memory access -------------------------------------------------------
-// Every load and store carries an L2 eviction-priority policy chosen per pass: the
-// input of a transform is read once (evict first), an intermediate that the next
-// pass reads back from L2 is kept (evict last), and the final result streams out
-// (evict first).
+// Every load and store carries an L2 eviction-priority policy chosen per pass: loads
+// are normal priority (reading with evict-first made the in-place column passes,
+// which write back the lines they read, 1-7% slower), an intermediate that the next
+// pass reads back from L2 is kept (evict last, chunked schedules), and the final
+// result streams out (evict first).
 __device__ __forceinline__ unsigned long long l2_policy(int kind) {
   unsigned long long pol;
   if (kind == 1) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
