@@ -718,12 +718,57 @@ def run_e2e(args, parts, host, device, fwt, world):
     per_step = [max((ends[p][i - 1] if i else t0).elapsed_time(ends[p][i]) for p in range(len(streams)))
                 for i in range(args.e2e_steps)]
     vectors = sum(w.batch for w in parts) * world * args.e2e_steps
+    floor = copies_only(args, pin_in, pin_out, device)
     return {"value": round(vectors / (ms / 1e3), 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": h2d, "steps": args.e2e_steps, "warmup": max(3, args.warmup),
             "ms_per_step": round(ms / args.e2e_steps, 3),
             "step_ms": {"median": round(statistics.median(per_step), 3), "min": round(min(per_step), 3),
                         "max": round(max(per_step), 3)},
+            "copies_only": floor,
             "workspace_bytes": sum(ws_each), "streams": len(streams)}
+
+
+def copies_only(args, pin_in, pin_out, device):
+    """The host link's floor for the same step: the same bytes copied host -> device on
+    one stream and device -> host on another (whole arrays, no transform), timed like the
+    end-to-end steps.  Its per-step median against e2e's shows how much of the link time
+    the pipelined transform adds; long steps in both come from the link, not the pipeline."""
+    import torch
+
+    # separate device buffers for the two directions, so the concurrent copies touch
+    # disjoint memory
+    dbuf = [(torch.empty_like(a, device=device), torch.empty_like(b, device=device)) for a, b in pin_in]
+    dsrc = [(torch.zeros_like(a, device=device), torch.zeros_like(b, device=device)) for a, b in pin_in]
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    main = torch.cuda.current_stream(device)
+
+    def step():
+        s_in.wait_stream(main)
+        s_out.wait_stream(main)
+        with torch.cuda.stream(s_in):
+            for (a, b), (da, db) in zip(pin_in, dbuf):
+                da.copy_(a, non_blocking=True)
+                db.copy_(b, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            for (ha, hb), (da, db) in zip(pin_out, dsrc):
+                ha.copy_(da, non_blocking=True)
+                hb.copy_(db, non_blocking=True)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.e2e_steps + 1)]
+    ev[0].record(main)
+    for i in range(args.e2e_steps):
+        step()
+        ev[i + 1].record(main)
+    torch.cuda.synchronize(device)
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.e2e_steps)]
+    del dbuf, dsrc
+    return {"ms_per_step": round(sum(per) / len(per), 3), "median_ms": round(statistics.median(per), 3),
+            "max_ms": round(max(per), 3)}
 
 
 def oracle_step(orc, parts, host, threads):
