@@ -21,7 +21,7 @@
 // fp64 runs its butterflies exactly in 64-bit fixed point on the integer units
 // (GB300's fp64 add rate is about 1/64 of its fp32 rate, while 64-bit integer
 // adds run near the fp32 rate): the tile's largest binary exponent sets a common
-// scale, every element is converted to an int64 with 61 - K fraction bits (integer
+// scale, every element is converted to an int64 with min(61 - K, 51) fraction bits (integer
 // bit arithmetic), the K stages run exactly, and each result is rounded once back
 // to fp64 (the hardware int64 -> fp64 conversion, round to nearest even, then an
 // exponent-field add; an all-integer exact rounding where results could be
@@ -564,7 +564,11 @@ __device__ __forceinline__ void fixed_tile(const PassParams& p, unsigned char* s
     return;
   }
   const int emax = max((int)(key >> 20), 1);  // zeros and subnormals scale as exponent 1
-  const int F = 61 - bits.tk;  // headroom: |q| <= 2^(F+1) grows by 2^tk
+  // Fraction bits: headroom for the growth (|q| <= 2^(F+1) grows by 2^tk), at most 51 so
+  // that every element shifts right and passes over few bits take the truncating
+  // conversion too (their error bound sqrt(T) 2^-51 stays far below the specification;
+  // measured 7-16% faster for factors of 4 to 9 bits than 61 - tk with the general form).
+  const int F = min(61 - bits.tk, 51);
   // (uniform branches) Tiles of up to 2^13 transformed elements truncate: their error
   // bound sqrt(T) 2^-F stays far below the fp64 specification; tiles of 2^14 round.
   bool converted = false;
