@@ -139,10 +139,10 @@ bool plan_valid(int n, int dtype, const Plan& p) {
 // split, column width and TMA mode at 2^26 elements a part for n <= 23, rechecked at
 // 2^28 for n = 18..23, of every split and width at 2^28 for larger n, and of every
 // fp64 three-factor split with TMA staging chosen per factor for n = 26..30).
-//  * fp64 n = 15..22: a row factor of 9..12 bits and a column factor of 6..11 at 32-
-//    (n = 21), 64- or 128-byte segments, every column tile staged by TMA (the TMA
-//    column kernel runs three CTAs an SM; the direct one two): passes of few bits are
-//    HBM-bound (~6.7 TB/s), 15-25% faster than the general rule.
+//  * fp64 n = 15..22: a row factor of 9..12 bits and a column factor of 6..10 at 64-
+//    or 128-byte segments, every column tile staged by TMA (the TMA column kernel runs
+//    three CTAs an SM; the direct one two): passes of few bits are HBM-bound
+//    (~6.7 TB/s), 15-25% faster than the general rule; n = 23: (12, 11) at 32 bytes.
 //  * 4-byte n = 18..23: 128-byte column segments (2-4% faster; at n = 23 the 9-bit
 //    column factor staged by TMA).
 //  * 4-byte n = 25, 26: an 11-bit column factor at 32 bytes; from n = 27 three
@@ -163,7 +163,7 @@ constexpr MeasuredSplit kMeasuredSplits[] = {
     {true, 15, 2, {9, 6, 0}, 128, 0b10},    {true, 16, 2, {10, 6, 0}, 128, 0b10},
     {true, 17, 2, {10, 7, 0}, 128, 0b10},   {true, 18, 2, {10, 8, 0}, 128, 0b10},
     {true, 19, 2, {12, 7, 0}, 128, 0b10},   {true, 20, 2, {12, 8, 0}, 128, 0b10},
-    {true, 21, 2, {11, 10, 0}, 32, 0b10},   {true, 22, 2, {12, 10, 0}, 64, 0b10},
+    {true, 21, 2, {12, 9, 0}, 64, 0b10},    {true, 22, 2, {12, 10, 0}, 64, 0b10},
     {true, 23, 2, {12, 11, 0}, 32, 0},
     {false, 18, 2, {12, 6, 0}, 128, 0}, {false, 19, 2, {13, 6, 0}, 128, 0},
     {false, 20, 2, {13, 7, 0}, 128, 0}, {false, 21, 2, {13, 8, 0}, 128, 0},
