@@ -13,6 +13,15 @@ multi-pass Kronecker path.
 
 Multi-GPU runs (torchrun, one rank per GPU) replicate the per-rank workload
 with no collective on the data path (weak scaling); rank 0 prints one JSON line.
+
+The line: `value` (vectors/s, inputs resident in HBM), `kernels` (per-pass device
+times from the library's event trace), `roofline` (the dominant pass against the
+measured copy bandwidth, with its ncu DRAM traffic while the sources match the
+committed capture), `per_config` (every specified shape on its own, beside the
+time of a plain streaming kernel over the same bytes, and checked against the CPU
+oracle), `e2e` (the same metric from pinned host arrays through the host-buffer
+entry points, beside plain copies of the same bytes), `cpu_baseline` (the oracle on
+the host cores) and `clocks` (sampled during the timed region).
 """
 from __future__ import annotations
 
